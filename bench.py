@@ -1,0 +1,385 @@
+#!/usr/bin/env python
+"""Benchmark of the TDT loss forward+backward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one call of the C ABI (node tables, alpha, beta, reduction,
+gradient) over one batch of the workload, inputs already in HBM.  L2 is
+flushed (a 2x-L2 buffer is written) between timed steps, outside the events.
+Prints one JSON line (rank 0).  ``value`` is achieved HBM throughput over the
+algorithmic bytes of the step (valid-node logits read once + every gradient
+element written once); ``ms_per_step`` the time of one step.
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+loss shards by utterance; there is no exchange on the path): weak scaling,
+value = bytes of all ranks / max-over-ranks time.
+
+``--impl reference`` times the CPU oracle (float64 C, OpenMP) on a bounded
+sample of the same workload on the host cores; the other ranks exit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from transducer_loss_asr_gb300.workloads import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = ("TDT loss fwd+bwd ms and achieved HBM GB/s (% of roofline) at "
+          "B4·T200·U40·V8193")
+ELT = {"f32": 4, "f16": 2, "bf16": 2}
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM bytes (read + write) per launch of the dominant kernel from one ncu
+# capture, valid only while the kernel source has this sha256.
+NCU_TRAFFIC = {}
+
+
+def algorithmic_bytes(inp):
+    """Valid-node logits read once + every gradient element written once."""
+    w = inp["workload"]
+    tl = inp["logit_lens"].cpu().numpy()
+    ul = inp["label_lens"].cpu().numpy()
+    elt = ELT[w.dtype]
+    valid_rows = int(np.sum(np.minimum(tl, w.T) * (np.minimum(ul, w.U) + 1)))
+    all_rows = w.B * w.T * (w.U + 1)
+    return valid_rows * w.VD * elt, all_rows * w.VD * elt, valid_rows, all_rows
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+
+    def stop(self):
+        if self.proc is None:
+            return
+        time.sleep(0.06)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def source_sha(name):
+    p = os.path.join(ROOT, "transducer_loss_asr_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def oracle_sample(inp, max_utts=1, frames=None):
+    """The oracle on the first utterance(s) of the workload, float32 up-cast;
+    ``frames`` keeps only that many leading frames (a smaller bounded sample)."""
+    import oracle
+
+    w = inp["workload"]
+    b = min(max_utts, w.B)
+    T = w.T if frames is None else max(1, min(frames, w.T))
+    z = inp["logits"][:b, :T].float().cpu().numpy()
+    labels = inp["labels"][:b].cpu().numpy()
+    tl = np.minimum(inp["logit_lens"][:b].cpu().numpy(), T)
+    ul = inp["label_lens"][:b].cpu().numpy()
+    elt = ELT[w.dtype]
+    valid = int(np.sum(tl * (ul + 1)))
+    sample_bytes = valid * w.VD * elt + b * T * (w.U + 1) * w.VD * elt
+    oracle.build()
+
+    def run():
+        oracle.tdt_loss(z, labels, tl, ul, inp["durations"], inp["blank"], inp["sigma"],
+                        inp["reduction"])
+
+    return run, sample_bytes, "%d of %d utterances, %d of %d frames (%d lattice rows of %d)" % (
+        b, w.B, T, w.T, valid, w.B * w.T * (w.U + 1))
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    inp = make_inputs(w, device="cpu")
+    run, sample_bytes, desc = oracle_sample(inp)
+    t0 = time.perf_counter()
+    run()
+    t1 = time.perf_counter() - t0
+    budget = 120.0  # seconds for warmup + timed steps
+    if (args.steps + args.warmup) * t1 > budget:
+        frames = int(w.T * budget / ((args.steps + args.warmup) * t1))
+        run, sample_bytes, desc = oracle_sample(inp, frames=frames)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = sample_bytes / dt / 1e9
+    cores = host_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, "oracle on host cores"),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_dict(w, l2):
+    return {"workload": "%s: B%d T%d U%d V%d D%d %s [%d,%d,%d,%d]%s, sigma %g, %s" % (
+        w.name, w.B, w.T, w.U, w.V, w.D, w.dtype, w.B, w.T, w.U + 1, w.VD,
+        " view of width %d" % w.base_vd if w.base_vd else "", w.sigma, w.reduction),
+        "lengths": "full" if w.T_range is None else "T_b in %s, U_b in %s" % (w.T_range,
+                                                                             w.U_range),
+        "l2": l2, "global_batch": w.B}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="parakeet", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+
+    from transducer_loss_asr_gb300 import binding
+
+    inp = make_inputs(w, device=dev, seed=w.seed + rank)
+    logits = inp["logits"]
+    read_b, write_b, valid_rows, all_rows = algorithmic_bytes(inp)
+    step_bytes = read_b + write_b
+    loss = torch.empty(w.B if w.reduction == "none" else 1, dtype=torch.float32, device=dev)
+    grad = torch.empty(logits.shape, dtype=logits.dtype, device=dev)
+
+    def step():
+        binding.tdt_loss_fwd_bwd(logits, inp["labels"], inp["logit_lens"], inp["label_lens"],
+                                 inp["durations"], inp["blank"], inp["sigma"], inp["reduction"],
+                                 loss_out=loss, grad_out=grad)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if local == 0 else None
+    binding.tdt_loss_timing_read(reset=True)
+    binding.tdt_loss_timing_enable(True)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.start()
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        starts[i].record()
+        step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    if sampler:
+        sampler.stop()
+    binding.tdt_loss_timing_enable(False)
+    kt = binding.tdt_loss_timing_read(reset=True)
+    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * step_bytes * args.steps / (total_ms / 1e3) / 1e9
+
+    # end to end through host buffers: inputs H2D, the call, loss + grad D2H
+    e2e_steps = args.e2e_steps or min(args.steps, 20)
+    base = logits._base if logits._base is not None else logits
+    base_h = torch.empty(base.shape, dtype=base.dtype, pin_memory=True)
+    base_h.copy_(base)
+    base_d = torch.empty_like(base)
+    view_d = base_d[..., : w.VD] if base is not logits else base_d
+    labels_h = inp["labels"].cpu().pin_memory()
+    tl_h = inp["logit_lens"].cpu().pin_memory()
+    ul_h = inp["label_lens"].cpu().pin_memory()
+    labels_d, tl_d, ul_d = (torch.empty_like(inp["labels"]), torch.empty_like(inp["logit_lens"]),
+                            torch.empty_like(inp["label_lens"]))
+    loss_h = torch.empty(loss.shape, dtype=loss.dtype, pin_memory=True)
+    grad_h = torch.empty(grad.shape, dtype=grad.dtype, pin_memory=True)
+    h2d = (base_h.numel() * base_h.element_size() + labels_h.numel() * 8 + tl_h.numel() * 8
+           + ul_h.numel() * 8)
+    d2h = loss_h.numel() * 4 + grad_h.numel() * grad_h.element_size()
+
+    def e2e_step():
+        base_d.copy_(base_h, non_blocking=True)
+        labels_d.copy_(labels_h, non_blocking=True)
+        tl_d.copy_(tl_h, non_blocking=True)
+        ul_d.copy_(ul_h, non_blocking=True)
+        binding.tdt_loss_fwd_bwd(view_d, labels_d, tl_d, ul_d, inp["durations"], inp["blank"],
+                                 inp["sigma"], inp["reduction"], loss_out=loss, grad_out=grad)
+        loss_h.copy_(loss, non_blocking=True)
+        grad_h.copy_(grad, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    e0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = torch.tensor([e0.elapsed_time(e1) / e2e_steps], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(e2e_ms, op=dist.ReduceOp.MAX)
+    e2e_value = world * step_bytes / (float(e2e_ms.item()) / 1e3) / 1e9
+    assert torch.equal(loss_h, loss.cpu())
+
+    # roofline of the dominant kernel (live per-kernel events over the timed region)
+    per_kernel = {k: {"ms_per_launch": (ms / n if n else 0.0), "launches": n}
+                  for k, (ms, n) in kt.items()}
+    dom = max(kt, key=lambda k: kt[k][0])
+    ms_dom, n_dom = kt[dom]
+    kbytes = {"grad": read_b + write_b, "node_tables": read_b}
+    peak, peak_kind = measured_peaks()
+    roofline = None
+    if dom in kbytes and n_dom:
+        achieved = kbytes[dom] / (ms_dom / n_dom / 1e3) / 1e9
+        src = {"grad": "tdt_grad.cu", "node_tables": "tdt_tables.cu"}[dom]
+        tr = NCU_TRAFFIC.get((dom, w.name))
+        traffic = tr["bytes"] if tr and tr["sha256"] == source_sha(src) else None
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                    "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                    "peak_source": peak_kind + " hbm_gbs (copy)"}
+    step_frac = (step_bytes / (ms_per_step / 1e3) / 1e9) / peak
+
+    cpu = None
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        run, sample_bytes, desc = oracle_sample(inp)
+        run()  # warm: build + page in
+        reps, t0 = 0, time.perf_counter()
+        while reps < 3 or time.perf_counter() - t0 < 10.0:
+            run()
+            reps += 1
+            if time.perf_counter() - t0 > 30.0:
+                break
+        dt = (time.perf_counter() - t0) / reps
+        cpu = {"value": sample_bytes / dt / 1e9, "unit": "GB/s", "cores": host_cores(),
+               "kind": "oracle", "sample": desc + ", %d runs, %.2f s each" % (reps, dt)}
+
+    if rank == 0:
+        clocks = sampler.summary() if sampler else None
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic",
+            "config": config_dict(w, "flushed between timed steps (2x L2 write)"),
+            "frac_of_hbm_roofline": step_frac,
+            "algorithmic_bytes_per_step": step_bytes,
+            "roofline": roofline,
+            "kernels": per_kernel,
+            "gpu_launches": int(sum(n for _, n in kt.values())),
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": float(e2e_ms.item()),
+                    "steps": e2e_steps},
+            "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,163 @@
+/*
+ * tdt_loss.h -- C ABI of the GB300 (sm_103a) Token-and-Duration Transducer
+ * (TDT) loss: forward and backward in one call.
+ *
+ * The operation ("tdt-loss: add TDT loss kernel", kernels-community PR
+ * #882, list "What's in it"):
+ *   - a log-softmax over the vocabulary at every lattice node, and one over
+ *     the duration logits;
+ *   - alpha/beta passes over the (t,u) lattice with 64-bit accumulation, no
+ *     limit of 1024 labels;
+ *   - one fused pass that writes the gradient w.r.t. the token and the
+ *     duration logits;
+ *   - fp32/fp16/bf16 logits read directly, including a slice
+ *     logits[..., :V+D] of a wider tensor, without a copy;
+ *   - the reductions mean_volume, mean_batch, mean, sum, none.
+ * sigma, the logit under-normalisation, is a loss parameter ("Add TDT loss
+ * kernel", transformers PR #46048, review: "test for sigma != 0").
+ *
+ * Lattice (published TDT, Xu et al. 2023): node (t,u), t < T_b, u <= U_b;
+ * blank arc (t,u)->(t+d,u) for d > 0; label arc (t,u)->(t+d,u+1) for every
+ * d incl. 0, landing before frame T_b; a path ends with a blank arc from
+ * (t,U_b) that lands exactly on T_b.  Arc weight = token log-prob - sigma +
+ * duration log-prob.  L_b = -log(sum over paths of exp(path weight)).
+ *
+ * Conventions common to every entry point
+ *   logits      device, [B, T, U+1, V+D] of `dtype`, addressed with the
+ *               element strides `strides` (strides[3] must be 1; the other
+ *               strides are free, e.g. a slice of a [..., W] tensor with
+ *               W > V+D).  Token logits are [..., 0:V) with `blank` inside,
+ *               duration logits [..., V:V+D), D = n_dur.
+ *   sizes       host, {B, T, U+1, V+D}; B >= 0, T >= 1, U+1 >= 1,
+ *               V+D > n_dur, T + U + 1 <= 65536.
+ *   labels      device int64 [B, U] contiguous (U = sizes[2]-1); entries at
+ *               u >= label_lens[b] are ignored (-100 padding).  May be NULL
+ *               when U = 0.
+ *   logit_lens  device int64 [B]: T_b.     label_lens: device int64 [B]: U_b.
+ *   durations   host int32 [n_dur], distinct, 0 <= d <= 255; 1 <= n_dur <= 32.
+ *   blank       index of blank in [0, V).
+ *   sigma       under-normalisation, |sigma| <= 1024.
+ *   reduction   one of TDT_REDUCTION_*.
+ *   loss_out    device float32: [B] for TDT_REDUCTION_NONE, else [1]
+ *               (NULL allowed only for B = 0 with TDT_REDUCTION_NONE).
+ *   grad_out    device, contiguous [B, T, U+1, V+D] of `dtype`; the
+ *               gradient of the reduced loss for an upstream gradient of 1
+ *               (of sum_b L_b for NONE).  NULL computes the loss only.
+ *               Rows outside an utterance's lattice are written as 0.
+ *   stream      a cudaStream_t (NULL: the legacy default stream).
+ * Memory: the caller owns every pointer; the library never frees them.
+ * Calls are asynchronous on `stream`: results are valid once the stream
+ * reaches them.  No call synchronises the device.
+ * Errors: a negative TDT_ERR_* status is returned before anything is
+ * enqueued when an argument is invalid.  Problems that only the device can
+ * see never trap: an utterance with T_b < 1, T_b > T, U_b < 0, U_b > U, or a
+ * used label outside [0,V) or equal to blank gets a NaN loss and zero
+ * gradient rows; an utterance with no complete path gets +inf and zero rows.
+ * Log-probabilities below -4096 are clamped to -4096 (exp(-4096) is far
+ * below the float64 range).
+ */
+#ifndef TDT_LOSS_H
+#define TDT_LOSS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TDT_LOSS_VERSION 1
+
+/* element type of logits and grad_out */
+#define TDT_DTYPE_F32 0
+#define TDT_DTYPE_F16 1
+#define TDT_DTYPE_BF16 2
+
+/* reductions ("supports all reductions: mean_volume, mean_batch, mean, sum, none") */
+#define TDT_REDUCTION_NONE 0        /* loss_out[b] = L_b                          */
+#define TDT_REDUCTION_SUM 1         /* sum_b L_b                                  */
+#define TDT_REDUCTION_MEAN 2        /* (1/B) sum_b L_b / U_b                      */
+#define TDT_REDUCTION_MEAN_BATCH 3  /* (1/B) sum_b L_b                            */
+#define TDT_REDUCTION_MEAN_VOLUME 4 /* sum_b L_b / sum_b U_b                      */
+
+/* status codes */
+#define TDT_OK 0
+#define TDT_ERR_NULL_POINTER (-1)
+#define TDT_ERR_BAD_SIZES (-2)
+#define TDT_ERR_BAD_STRIDES (-3)
+#define TDT_ERR_BAD_DTYPE (-4)
+#define TDT_ERR_BAD_DURATIONS (-5)
+#define TDT_ERR_BAD_BLANK (-6)
+#define TDT_ERR_BAD_REDUCTION (-7)
+#define TDT_ERR_BAD_SIGMA (-8)
+#define TDT_ERR_WORKSPACE_TOO_SMALL (-9)
+#define TDT_ERR_CUDA (-10)
+#define TDT_ERR_BAD_ALIGNMENT (-11)
+
+/*
+ * Loss and gradient in one call.  Internal scratch (per-node tables, alpha,
+ * beta; tdt_loss_workspace_size bytes) is taken from the stream-ordered
+ * allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
+ * Returns TDT_OK or a TDT_ERR_* status.
+ */
+int tdt_loss_fwd_bwd(const void *logits, const int64_t sizes[4], const int64_t strides[4],
+                     int dtype, const int64_t *labels, const int64_t *logit_lens,
+                     const int64_t *label_lens, const int32_t *durations, int n_dur, int blank,
+                     double sigma, int reduction, float *loss_out, void *grad_out, void *stream);
+
+/*
+ * Bytes of device scratch that tdt_loss_fwd_bwd_ws needs for these sizes
+ * (0 for invalid arguments).  The value depends only on sizes and n_dur.
+ */
+size_t tdt_loss_workspace_size(const int64_t sizes[4], int n_dur);
+
+/*
+ * Same as tdt_loss_fwd_bwd, with caller-owned scratch: `workspace` is a
+ * device pointer, 256-byte aligned, of at least workspace_bytes >=
+ * tdt_loss_workspace_size(sizes, n_dur) bytes, not used by anything else
+ * until the stream has passed this call.  Nothing is allocated.
+ */
+int tdt_loss_fwd_bwd_ws(const void *logits, const int64_t sizes[4], const int64_t strides[4],
+                        int dtype, const int64_t *labels, const int64_t *logit_lens,
+                        const int64_t *label_lens, const int32_t *durations, int n_dur,
+                        int blank, double sigma, int reduction, float *loss_out,
+                        void *grad_out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Benchmark support (not needed for correctness).  Kernel ids, in launch
+ * order: node tables, alpha, beta, reduction, gradient.
+ */
+#define TDT_KERNEL_TABLES 0
+#define TDT_KERNEL_ALPHA 1
+#define TDT_KERNEL_BETA 2
+#define TDT_KERNEL_REDUCE 3
+#define TDT_KERNEL_GRAD 4
+#define TDT_KERNEL_COUNT 5
+
+/*
+ * on != 0: every later call records a CUDA event pair around each of its
+ * kernels, on the stream that kernel is launched on; on == 0 stops it.
+ * Process-wide; not meant for stream capture.
+ */
+void tdt_loss_timing_enable(int on);
+
+/*
+ * Sum of the recorded kernel durations in milliseconds (ms_out) and the
+ * number of launches (count_out) per kernel id, for the first n ids, since
+ * the last reset.  Blocks until the recorded events have completed.
+ * reset != 0 clears the sums afterwards.  Returns the number of ids written
+ * or TDT_ERR_CUDA.
+ */
+int tdt_loss_timing_read(double *ms_out, int64_t *count_out, int n, int reset);
+
+/* Human-readable text for a status code (static storage). */
+const char *tdt_status_string(int status);
+
+/* TDT_LOSS_VERSION of the loaded library. */
+int tdt_loss_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TDT_LOSS_H */

@@ -1,0 +1,265 @@
+"""GPU (C ABI) versus the CPU oracle, element by element.
+
+Tolerances (fp32 logits): loss relative error <= 1e-6, gradient absolute
+error <= 1e-5.  bf16/fp16 logits: loss relative <= 2e-3, gradient absolute
+<= 2e-2, against the oracle run on the same up-cast inputs; bf16/fp16 are
+also held to a tighter bound, one unit in the last place of the stored
+gradient plus 2e-6, since the kernels compute in fp32 and round once.
+"""
+import numpy as np
+import pytest
+import torch
+
+from transducer_loss_asr_gb300.workloads import WORKLOADS, make_inputs, scaled
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": (1e-6, 1e-5), "f16": (2e-3, 2e-2), "bf16": (2e-3, 2e-2)}
+ULP = {"f16": 2.0 ** -10, "bf16": 2.0 ** -7}
+
+
+@pytest.fixture(scope="module")
+def binding():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from transducer_loss_asr_gb300 import binding as b
+
+    return b
+
+
+def run_gpu(binding, inp, compute_grad=True):
+    loss, grad = binding.tdt_loss_fwd_bwd(
+        inp["logits"], inp["labels"], inp["logit_lens"], inp["label_lens"], inp["durations"],
+        inp["blank"], inp["sigma"], inp["reduction"], compute_grad=compute_grad)
+    torch.cuda.synchronize()
+    return loss, grad
+
+
+def run_oracle(oracle_mod, inp, rows=None, want_grad=True):
+    return oracle_mod.tdt_loss(
+        inp["logits"].float().cpu().numpy(), inp["labels"].cpu().numpy(),
+        inp["logit_lens"].cpu().numpy(), inp["label_lens"].cpu().numpy(), inp["durations"],
+        inp["blank"], inp["sigma"], inp["reduction"], want_grad=want_grad, rows=rows)
+
+
+def check_loss(l_gpu, l_ref, dtype):
+    rtol = TOL[dtype][0]
+    l_gpu = l_gpu.double().cpu().numpy()
+    fin = np.isfinite(l_ref)
+    assert np.array_equal(np.isnan(l_gpu), np.isnan(l_ref))
+    assert np.array_equal(np.isposinf(l_gpu), np.isposinf(l_ref))
+    rel = np.abs(l_gpu[fin] - l_ref[fin]) / np.maximum(np.abs(l_ref[fin]), 1e-30)
+    assert rel.size == 0 or rel.max() <= rtol, "loss rel err %.3e > %.1e" % (rel.max(), rtol)
+    return rel.max() if rel.size else 0.0
+
+
+def check_grad(g_gpu, g_ref, dtype, chunk=1 << 24):
+    """Compare in chunks of the flattened arrays to bound host memory."""
+    atol = TOL[dtype][1]
+    g_flat = g_gpu.reshape(-1)
+    r_flat = g_ref.reshape(-1)
+    assert g_flat.numel() == r_flat.size
+    worst = 0.0
+    for s in range(0, r_flat.size, chunk):
+        g = g_flat[s:s + chunk].double().cpu().numpy()
+        r = r_flat[s:s + chunk]
+        err = np.abs(g - r)
+        worst = max(worst, float(err.max()) if err.size else 0.0)
+        assert not err.size or err.max() <= atol, "grad abs err %.3e > %.1e" % (err.max(), atol)
+        if dtype in ULP and err.size:
+            bound = np.abs(r) * ULP[dtype] + 2e-6
+            assert (err <= bound).all(), "grad beyond one ulp: %.3e" % (err - bound).max()
+    return worst
+
+
+def full_check(binding, oracle_mod, inp):
+    w = inp["workload"]
+    loss, grad = run_gpu(binding, inp)
+    ref = run_oracle(oracle_mod, inp)
+    check_loss(loss, ref.loss, w.dtype)
+    check_grad(grad, ref.grad, w.dtype)
+    return loss, grad, ref
+
+
+# ------------------------------------------------------------- small and medium
+
+def test_tiny_workload(binding, oracle_mod):
+    full_check(binding, oracle_mod, make_inputs("tiny", device="cuda"))
+
+
+MEDIUM = {
+    # several warp tiles per row, a ragged tail (V not a multiple of 256), ragged lengths
+    "f32_ragged_view": dict(B=3, T=37, U=11, V=1000, blank=999, durations=(0, 1, 2, 3, 4),
+                            dtype="f32", std=1.0, sigma=0.05, reduction="mean_volume",
+                            T_range=(20, 37), U_range=(3, 11), base_vd=1013),
+    "bf16_ragged_view": dict(B=4, T=29, U=9, V=777, blank=776, durations=(0, 1, 2, 3),
+                             dtype="bf16", std=1.5, sigma=0.1, reduction="mean",
+                             T_range=(10, 29), U_range=(1, 9), base_vd=790),
+    "f16_full": dict(B=2, T=18, U=6, V=513, blank=512, durations=(0, 1, 2), dtype="f16",
+                     std=1.0, sigma=0.0, reduction="sum"),
+    "f32_no_zero_duration": dict(B=2, T=25, U=5, V=64, blank=63, durations=(1, 2, 4),
+                                 dtype="f32", std=2.0, sigma=0.02, reduction="none",
+                                 T_range=(12, 25), U_range=(0, 5)),
+    "f32_unsorted_blank_first": dict(B=3, T=15, U=4, V=40, blank=0, durations=(3, 0, 1),
+                                     dtype="f32", std=1.0, sigma=0.0, reduction="mean_batch"),
+    "f32_long_rows": dict(B=1, T=9, U=3, V=20001, blank=20000, durations=(0, 1, 2, 3, 4),
+                          dtype="f32", std=1.0, sigma=0.0, reduction="sum"),
+    "f32_many_durations": dict(B=2, T=40, U=8, V=33, blank=32, durations=tuple(range(17)),
+                               dtype="f32", std=1.0, sigma=0.3, reduction="mean_volume"),
+    "f32_labels_past_1024": dict(B=1, T=300, U=1100, V=9, blank=8, durations=(0, 1, 2),
+                                 dtype="f32", std=1.0, sigma=0.0, reduction="none"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MEDIUM))
+def test_medium_cases(binding, oracle_mod, name):
+    w = scaled(WORKLOADS["tiny"], name=name, seed=777, **MEDIUM[name])
+    full_check(binding, oracle_mod, make_inputs(w, device="cuda"))
+
+
+@pytest.mark.parametrize("red", ["none", "sum", "mean", "mean_batch", "mean_volume"])
+def test_every_reduction(binding, oracle_mod, red):
+    w = scaled(WORKLOADS["tiny"], name="red_" + red, B=5, T=14, U=5, V=50, blank=49,
+               durations=(0, 1, 2), sigma=0.05, reduction=red, T_range=(6, 14), U_range=(1, 5),
+               seed=31)
+    full_check(binding, oracle_mod, make_inputs(w, device="cuda"))
+
+
+# ------------------------------------------------------------- edge cases
+
+def test_empty_batch(binding):
+    for red, expect in (("sum", 0.0), ("mean_batch", np.nan), ("none", None)):
+        z = torch.zeros(0, 5, 3, 10, device="cuda")
+        e = torch.zeros(0, dtype=torch.int64, device="cuda")
+        loss, grad = binding.tdt_loss_fwd_bwd(z, torch.zeros(0, 2, dtype=torch.int64,
+                                                             device="cuda"), e, e, [0, 1, 2], 6,
+                                              0.0, red)
+        torch.cuda.synchronize()
+        if expect is None:
+            assert loss.numel() == 0
+        elif np.isnan(expect):
+            assert torch.isnan(loss).all()
+        else:
+            assert loss.item() == expect
+        assert grad.numel() == 0
+
+
+def test_no_labels_at_all(binding, oracle_mod):
+    w = scaled(WORKLOADS["tiny"], name="no_labels", U=0, T=11, durations=(0, 1, 2),
+               V=7, blank=6, reduction="sum", seed=5)
+    full_check(binding, oracle_mod, make_inputs(w, device="cuda"))
+
+
+def test_degenerate_utterances(binding, oracle_mod):
+    """No path (+inf, zero rows), unusable lengths/labels (NaN, zero rows),
+    T_b = 1, U_b = 0, durations longer than the utterance."""
+    w = scaled(WORKLOADS["tiny"], name="degenerate", B=6, T=9, U=3, V=6, blank=5,
+               durations=(0, 2, 11), reduction="none", seed=8)
+    inp = make_inputs(w, device="cuda")
+    inp["logit_lens"] = torch.tensor([9, 8, 1, 9, 12, 4], device="cuda")   # 9 odd: no path
+    inp["label_lens"] = torch.tensor([3, 2, 0, 0, 1, 2], device="cuda")
+    labels = inp["labels"].clone()
+    labels[:, :] = 1
+    labels[1, 2:] = -100
+    labels[2, :] = -100
+    labels[3, :] = -100
+    labels[4, 1:] = -100
+    labels[5, 1] = 5     # blank used as a label -> unusable
+    labels[5, 2:] = -100
+    inp["labels"] = labels
+    loss, grad, ref = full_check(binding, oracle_mod, inp)
+    l = loss.cpu().numpy()
+    assert np.isposinf(l[0]) and np.isnan(l[4]) and np.isnan(l[5])
+    g = grad.cpu()
+    assert (g[0] == 0).all() and (g[4] == 0).all() and (g[5] == 0).all()
+
+
+def test_loss_only_matches(binding, oracle_mod):
+    inp = make_inputs(scaled(WORKLOADS["parakeet_bf16_ragged"], B=3, T=30, U=6, V=301,
+                             blank=300, base_vd=320, T_range=(12, 30), U_range=(2, 6)),
+                      device="cuda")
+    l1, g1 = run_gpu(binding, inp, compute_grad=False)
+    assert g1 is None
+    l2, g2 = run_gpu(binding, inp)
+    assert torch.equal(l1, l2)
+    ref = run_oracle(oracle_mod, inp, want_grad=False)
+    check_loss(l1, ref.loss, "bf16")
+
+
+def test_workspace_variant_and_determinism(binding):
+    inp = make_inputs(scaled(WORKLOADS["parakeet"], B=2, T=40, U=9, V=2049, blank=2048),
+                      device="cuda")
+    l1, g1 = run_gpu(binding, inp)
+    need = binding.tdt_loss_workspace_size(inp["logits"].shape, len(inp["durations"]))
+    ws = torch.full((need,), 0x7f, dtype=torch.uint8, device="cuda")
+    l2, g2 = binding.tdt_loss_fwd_bwd_ws(
+        inp["logits"], inp["labels"], inp["logit_lens"], inp["label_lens"], inp["durations"],
+        inp["blank"], ws, inp["sigma"], inp["reduction"])
+    torch.cuda.synchronize()
+    assert torch.equal(l1, l2) and torch.equal(g1, g2)
+    l3, g3 = run_gpu(binding, inp)
+    assert torch.equal(l1, l3) and torch.equal(g1, g3)
+
+
+def test_closed_form_long_lattice(binding):
+    """Uniform logits, durations [0, 1], T = 900, U = 1200: the exact loss is a
+    log-sum of binomial terms; pins the long fixed-point lattice on the GPU."""
+    from scipy.special import gammaln, logsumexp
+
+    T, U, V, sigma = 900, 1200, 4, 0.02
+    z = torch.zeros(1, T, U + 1, V + 2, device="cuda")
+    labels = torch.zeros(1, U, dtype=torch.int64, device="cuda")
+    tl = torch.tensor([T], device="cuda")
+    ul = torch.tensor([U], device="cuda")
+    loss, grad = binding.tdt_loss_fwd_bwd(z, labels, tl, ul, [0, 1], V - 1, sigma, "none")
+    torch.cuda.synchronize()
+    c = -np.log(V) - np.log(2) - sigma
+    ks = np.arange(0, min(U, T - 1) + 1)
+    terms = (gammaln(U + 1) - gammaln(ks + 1) - gammaln(U - ks + 1)
+             + gammaln(U + T - ks) - gammaln(U + 1) - gammaln(T - ks) + (U + T - ks) * c)
+    expect = -logsumexp(terms)
+    assert abs(loss.item() - expect) / expect <= 1e-6
+    rs = grad.double().sum(-1)
+    assert rs.abs().max().item() <= 1e-5
+
+
+# ------------------------------------------------------------- full-size workloads
+
+def _sample_rows(inp, n_random=1500, seed=0):
+    w = inp["workload"]
+    B, T, U1 = w.B, w.T, w.U + 1
+    tl = inp["logit_lens"].cpu().numpy()
+    ul = inp["label_lens"].cpu().numpy()
+    rng = np.random.default_rng(seed)
+    rows = set(rng.integers(0, B * T * U1, size=n_random).tolist())
+    for b in range(B):
+        for t in (0, 1, tl[b] - 1, min(tl[b], T - 1)):
+            for u in (0, 1, ul[b] - 1 if ul[b] > 0 else 0, ul[b], min(ul[b] + 1, U1 - 1)):
+                rows.add(int((b * T + t) * U1 + u))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["parakeet", "parakeet_bf16_ragged"])
+def test_full_size_parakeet(binding, oracle_mod, name):
+    inp = make_inputs(name, device="cuda")
+    base = inp["logits"]._base if inp["logits"]._base is not None else inp["logits"]
+    before = base.float().sum().item()
+    full_check(binding, oracle_mod, inp)
+    assert base.float().sum().item() == before   # the input (and its wider base) is untouched
+
+
+@pytest.mark.parametrize("name", ["large_batch", "long_labels"])
+def test_full_size_sampled(binding, oracle_mod, name):
+    inp = make_inputs(name, device="cuda")
+    w = inp["workload"]
+    loss, grad = run_gpu(binding, inp)
+    rows = _sample_rows(inp)
+    ref = run_oracle(oracle_mod, inp, rows=rows)
+    check_loss(loss, ref.loss, w.dtype)
+    g = grad.reshape(-1, w.VD)[torch.as_tensor(rows, device="cuda")]
+    check_grad(g, ref.grad, w.dtype)
+    # properties at every row: token and duration gradients each sum to 0
+    rs = grad.float().reshape(-1, w.VD)
+    tol = 1e-4 if w.dtype == "f32" else 5e-2
+    assert rs[:, : w.V].sum(-1).abs().max().item() <= tol
+    assert rs[:, w.V:].sum(-1).abs().max().item() <= tol

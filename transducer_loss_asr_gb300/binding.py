@@ -1,0 +1,172 @@
+"""ctypes binding of libtdt_loss.so (include/tdt_loss.h).
+
+Argument marshalling only: sizes, strides, dtype codes, raw pointers and the
+current CUDA stream go to the C ABI; every step of the loss runs in the
+library's kernels.  PyTorch is used for device memory and streams.  There is
+no fallback: if the library is missing, importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtdt_loss.so")
+
+DTYPES = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+REDUCTIONS = {"none": 0, "sum": 1, "mean": 2, "mean_batch": 3, "mean_volume": 4}
+
+TDT_OK = 0
+
+
+class TDTError(RuntimeError):
+    """A TDT_ERR_* status returned by the library."""
+
+    def __init__(self, status: int, text: str):
+        super().__init__("tdt_loss status %d: %s" % (status, text))
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            "libtdt_loss.so is not built (%s); run `python -m transducer_loss_asr_gb300.build` "
+            "or __graft_entry__.build()" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    common = [P, P, P, I, P, P, P, P, I, I, ctypes.c_double, I, P, P]
+    lib.tdt_loss_fwd_bwd.restype = I
+    lib.tdt_loss_fwd_bwd.argtypes = common + [P]
+    lib.tdt_loss_fwd_bwd_ws.restype = I
+    lib.tdt_loss_fwd_bwd_ws.argtypes = common + [P, ctypes.c_size_t, P]
+    lib.tdt_loss_workspace_size.restype = ctypes.c_size_t
+    lib.tdt_loss_workspace_size.argtypes = [P, I]
+    lib.tdt_status_string.restype = ctypes.c_char_p
+    lib.tdt_status_string.argtypes = [I]
+    lib.tdt_loss_version.restype = I
+    lib.tdt_loss_version.argtypes = []
+    lib.tdt_loss_timing_enable.restype = None
+    lib.tdt_loss_timing_enable.argtypes = [I]
+    lib.tdt_loss_timing_read.restype = I
+    lib.tdt_loss_timing_read.argtypes = [P, P, I, I]
+    return lib
+
+
+lib = _load()
+
+
+def status_string(status: int) -> str:
+    return lib.tdt_status_string(int(status)).decode()
+
+
+def _check(status: int):
+    if status != TDT_OK:
+        raise TDTError(status, status_string(status))
+
+
+def _i64(vals):
+    return (ctypes.c_int64 * 4)(*[int(v) for v in vals])
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def workspace_size(sizes, n_dur: int) -> int:
+    return int(lib.tdt_loss_workspace_size(_i64(sizes), int(n_dur)))
+
+
+def _marshal(logits, labels, logit_lens, label_lens, durations, blank, sigma, reduction,
+             loss_out, grad_out, compute_grad):
+    if logits.dim() != 4:
+        raise ValueError("logits must be [B, T, U+1, V+D]")
+    if logits.dtype not in DTYPES:
+        raise TypeError("logits dtype must be float32, float16 or bfloat16")
+    B = logits.shape[0]
+    dev = logits.device
+    if loss_out is None:
+        loss_out = torch.empty(B if reduction == "none" else 1, dtype=torch.float32, device=dev)
+    if compute_grad and grad_out is None:
+        grad_out = torch.empty(logits.shape, dtype=logits.dtype, device=dev)
+    if grad_out is not None and (not grad_out.is_contiguous() or grad_out.dtype != logits.dtype
+                                 or tuple(grad_out.shape) != tuple(logits.shape)):
+        raise ValueError("grad_out must be contiguous with the logits' shape and dtype")
+    durs = (ctypes.c_int32 * len(durations))(*[int(d) for d in durations])
+    args = [
+        _ptr(logits), _i64(logits.shape), _i64(logits.stride()), DTYPES[logits.dtype],
+        _ptr(labels) if labels is not None and labels.numel() > 0 else None,
+        _ptr(logit_lens), _ptr(label_lens), durs, len(durations), int(blank), float(sigma),
+        REDUCTIONS[reduction], _ptr(loss_out), _ptr(grad_out),
+    ]
+    for name, t in (("labels", labels), ("logit_lens", logit_lens), ("label_lens", label_lens)):
+        if t is not None and (t.dtype != torch.int64 or not t.is_contiguous() or t.device != dev):
+            raise ValueError("%s must be a contiguous int64 tensor on %s" % (name, dev))
+    return args, loss_out, grad_out
+
+
+def tdt_loss_fwd_bwd(logits, labels, logit_lens, label_lens, durations, blank, sigma=0.0,
+                     reduction="mean_volume", loss_out=None, grad_out=None, compute_grad=True):
+    """TDT loss and its gradient in one call on the current CUDA stream.
+
+    Returns (loss, grad): loss float32 [B] ("none") or [1]; grad with the
+    logits' shape and dtype (None when compute_grad is False and no grad_out
+    is given).  ``logits`` may be a strided view such as ``base[..., :V+D]``.
+    """
+    args, loss_out, grad_out = _marshal(logits, labels, logit_lens, label_lens, durations,
+                                        blank, sigma, reduction, loss_out, grad_out,
+                                        compute_grad)
+    with torch.cuda.device(logits.device):
+        _check(lib.tdt_loss_fwd_bwd(*args, _stream_handle(logits.device)))
+    return loss_out, grad_out
+
+
+def tdt_loss_fwd_bwd_ws(logits, labels, logit_lens, label_lens, durations, blank, workspace,
+                        sigma=0.0, reduction="mean_volume", loss_out=None, grad_out=None,
+                        compute_grad=True):
+    """As tdt_loss_fwd_bwd with a caller-owned uint8 CUDA workspace tensor."""
+    args, loss_out, grad_out = _marshal(logits, labels, logit_lens, label_lens, durations,
+                                        blank, sigma, reduction, loss_out, grad_out,
+                                        compute_grad)
+    with torch.cuda.device(logits.device):
+        _check(lib.tdt_loss_fwd_bwd_ws(*args, _ptr(workspace), workspace.numel(),
+                                       _stream_handle(logits.device)))
+    return loss_out, grad_out
+
+
+def tdt_loss_workspace_size(sizes, n_dur: int) -> int:
+    """Bytes of scratch tdt_loss_fwd_bwd_ws needs (0 for invalid sizes)."""
+    return workspace_size(sizes, n_dur)
+
+
+def tdt_status_string(status: int) -> str:
+    return status_string(status)
+
+
+def tdt_loss_version() -> int:
+    return int(lib.tdt_loss_version())
+
+
+KERNEL_NAMES = ("node_tables", "alpha", "beta", "reduce", "grad")
+
+
+def tdt_loss_timing_enable(on: bool) -> None:
+    """Record CUDA events around each kernel of later calls (benchmarks only)."""
+    lib.tdt_loss_timing_enable(1 if on else 0)
+
+
+def tdt_loss_timing_read(reset: bool = True):
+    """{kernel name: (summed ms, launches)} since the last reset; waits for the events."""
+    n = len(KERNEL_NAMES)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int64 * n)()
+    rc = lib.tdt_loss_timing_read(ms, cnt, n, 1 if reset else 0)
+    if rc < 0:
+        raise TDTError(rc, status_string(rc))
+    return {KERNEL_NAMES[i]: (ms[i], cnt[i]) for i in range(n)}

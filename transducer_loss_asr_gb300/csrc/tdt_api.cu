@@ -1,0 +1,295 @@
+// tdt_api.cu -- the C ABI (include/tdt_loss.h): argument checks, scratch
+// layout, and the order of the kernels on the caller's stream:
+//   K1 node tables -> K2 alpha -> K3 beta -> K5 reduction -> K4 gradient.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/tdt_loss.h"
+#include "tdt_common.cuh"
+
+namespace tdt {
+namespace {
+
+size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
+
+struct Layout {
+  size_t wb, wl, lpd, alpha, beta, lse_tok, lse_dur, frac, loglik, scale, usable, total;
+};
+
+bool make_layout(const int64_t sizes[4], int n_dur, Layout *L) {
+  if (!sizes) return false;
+  const long long B = sizes[0], T = sizes[1], U1 = sizes[2];
+  if (B < 0 || T < 1 || U1 < 1 || n_dur < 1 || n_dur > kMaxDurations) return false;
+  if (T + U1 > 65536) return false;
+  const size_t ndiag = (size_t)B * (size_t)(T + U1 - 1) * (size_t)U1;
+  const size_t nodes = (size_t)B * (size_t)T * (size_t)U1;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes);
+    return at;
+  };
+  L->wb = take(ndiag * 8);
+  L->wl = take(ndiag * 8);
+  L->lpd = take(ndiag * 8 * (size_t)n_dur);
+  L->alpha = take(ndiag * 8);
+  L->beta = take(ndiag * 8);
+  L->lse_tok = take(nodes * 4);
+  L->lse_dur = take(nodes * 4);
+  L->frac = take(nodes * 4 * (size_t)(2 + n_dur));
+  L->loglik = take((size_t)B * 8);
+  L->scale = take((size_t)B * 8);
+  L->usable = take((size_t)B * 4);
+  L->total = off > 0 ? off : 256;
+  return true;
+}
+
+Workspace carve(const Layout &L, void *base) {
+  char *c = static_cast<char *>(base);
+  Workspace w;
+  w.wb = reinterpret_cast<fx_t *>(c + L.wb);
+  w.wl = reinterpret_cast<fx_t *>(c + L.wl);
+  w.lpd = reinterpret_cast<fx_t *>(c + L.lpd);
+  w.alpha = reinterpret_cast<fx_t *>(c + L.alpha);
+  w.beta = reinterpret_cast<fx_t *>(c + L.beta);
+  w.lse_tok = reinterpret_cast<float *>(c + L.lse_tok);
+  w.lse_dur = reinterpret_cast<float *>(c + L.lse_dur);
+  w.frac = reinterpret_cast<float *>(c + L.frac);
+  w.loglik = reinterpret_cast<fx_t *>(c + L.loglik);
+  w.scale = reinterpret_cast<double *>(c + L.scale);
+  w.usable = reinterpret_cast<int *>(c + L.usable);
+  return w;
+}
+
+size_t elem_size(int dtype) { return dtype == TDT_DTYPE_F32 ? 4 : 2; }
+
+// Host-side validation; fills the kernel parameter block.  No device access.
+int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4], int dtype,
+             const int64_t *labels, const int64_t *logit_lens, const int64_t *label_lens,
+             const int32_t *durations, int n_dur, int blank, double sigma, int reduction,
+             const float *loss_out, const void *grad_out, Problem *p) {
+  if (!sizes || !strides || !durations) return TDT_ERR_NULL_POINTER;
+  // loss_out may be NULL only when it has no elements (empty batch, reduction none)
+  if (!loss_out && !(sizes[0] == 0 && reduction == TDT_REDUCTION_NONE)) return TDT_ERR_NULL_POINTER;
+  if (dtype != TDT_DTYPE_F32 && dtype != TDT_DTYPE_F16 && dtype != TDT_DTYPE_BF16)
+    return TDT_ERR_BAD_DTYPE;
+  if (n_dur < 1 || n_dur > kMaxDurations) return TDT_ERR_BAD_DURATIONS;
+  const long long B = sizes[0], T = sizes[1], U1 = sizes[2], VD = sizes[3];
+  if (B < 0 || T < 1 || U1 < 1 || VD <= n_dur) return TDT_ERR_BAD_SIZES;
+  if (T + U1 > 65536) return TDT_ERR_BAD_SIZES;
+  if (B > 0 && (!logits || !logit_lens || !label_lens)) return TDT_ERR_NULL_POINTER;
+  if (B > 0 && U1 > 1 && !labels) return TDT_ERR_NULL_POINTER;
+  if (strides[3] != 1 || strides[0] < 0 || strides[1] < 0 || strides[2] < 0)
+    return TDT_ERR_BAD_STRIDES;
+  int max_dur = 0;
+  for (int i = 0; i < n_dur; ++i) {
+    if (durations[i] < 0 || durations[i] > kMaxDurationValue) return TDT_ERR_BAD_DURATIONS;
+    for (int j = 0; j < i; ++j)
+      if (durations[j] == durations[i]) return TDT_ERR_BAD_DURATIONS;
+    if (durations[i] > max_dur) max_dur = durations[i];
+  }
+  const long long V = VD - n_dur;
+  if (blank < 0 || blank >= V) return TDT_ERR_BAD_BLANK;
+  if (reduction < TDT_REDUCTION_NONE || reduction > TDT_REDUCTION_MEAN_VOLUME)
+    return TDT_ERR_BAD_REDUCTION;
+  if (!(fabs(sigma) <= 1024.0)) return TDT_ERR_BAD_SIGMA;
+  const size_t es = elem_size(dtype);
+  if (((uintptr_t)logits % es) != 0 || (grad_out && ((uintptr_t)grad_out % es) != 0) ||
+      ((uintptr_t)loss_out % 4) != 0)
+    return TDT_ERR_BAD_ALIGNMENT;
+
+  memset(p, 0, sizeof(*p));
+  p->logits = logits;
+  p->B = B; p->T = T; p->U1 = U1; p->VD = VD; p->V = V; p->D = n_dur;
+  p->s0 = strides[0]; p->s1 = strides[1]; p->s2 = strides[2];
+  p->labels = reinterpret_cast<const long long *>(labels);
+  p->logit_lens = reinterpret_cast<const long long *>(logit_lens);
+  p->label_lens = reinterpret_cast<const long long *>(label_lens);
+  for (int i = 0; i < n_dur; ++i) p->dur[i] = durations[i];
+  p->n_dur = n_dur;
+  p->max_dur = max_dur;
+  p->blank = blank;
+  p->reduction = reduction;
+  p->sigma_fx = (fx_t)llround(sigma * kFxOne);
+  p->n_diag = T + U1 - 1;
+  return TDT_OK;
+}
+
+// ---- optional per-kernel timing (benchmarks) --------------------------------
+struct Timing {
+  std::mutex mu;
+  bool on = false;
+  struct Pending { int id; cudaEvent_t a, b; };
+  std::vector<Pending> pending;
+  std::vector<cudaEvent_t> pool;
+  double ms[TDT_KERNEL_COUNT] = {0};
+  long long count[TDT_KERNEL_COUNT] = {0};
+};
+Timing &timing() {
+  static Timing t;
+  return t;
+}
+cudaEvent_t take_event(Timing &t) {
+  if (!t.pool.empty()) {
+    cudaEvent_t e = t.pool.back();
+    t.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
+// Launch one kernel through `fn`, bracketed by events when timing is on.
+template <class F>
+cudaError_t timed(int id, cudaStream_t stream, F fn) {
+  Timing &t = timing();
+  bool on;
+  {
+    std::lock_guard<std::mutex> g(t.mu);
+    on = t.on;
+  }
+  if (!on) return fn();
+  cudaEvent_t a, b;
+  {
+    std::lock_guard<std::mutex> g(t.mu);
+    a = take_event(t);
+    b = take_event(t);
+  }
+  cudaEventRecord(a, stream);
+  cudaError_t e = fn();
+  cudaEventRecord(b, stream);
+  std::lock_guard<std::mutex> g(t.mu);
+  t.pending.push_back({id, a, b});
+  return e;
+}
+
+int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void *grad_out,
+        cudaStream_t stream) {
+  if (timed(TDT_KERNEL_TABLES, stream,
+            [&] { return launch_node_tables(p, dtype, ws, stream); }) != cudaSuccess)
+    return TDT_ERR_CUDA;
+  if (timed(TDT_KERNEL_ALPHA, stream, [&] { return launch_alpha(p, ws, stream); }) !=
+      cudaSuccess)
+    return TDT_ERR_CUDA;
+  if (grad_out &&
+      timed(TDT_KERNEL_BETA, stream, [&] { return launch_beta(p, ws, stream); }) != cudaSuccess)
+    return TDT_ERR_CUDA;
+  if (timed(TDT_KERNEL_REDUCE, stream,
+            [&] { return launch_reduce(p, ws, loss_out, stream); }) != cudaSuccess)
+    return TDT_ERR_CUDA;
+  if (grad_out && timed(TDT_KERNEL_GRAD, stream, [&] {
+        return launch_grad(p, dtype, ws, grad_out, stream);
+      }) != cudaSuccess)
+    return TDT_ERR_CUDA;
+  return TDT_OK;
+}
+
+}  // namespace
+}  // namespace tdt
+
+extern "C" {
+
+size_t tdt_loss_workspace_size(const int64_t sizes[4], int n_dur) {
+  tdt::Layout L;
+  if (!tdt::make_layout(sizes, n_dur, &L)) return 0;
+  return L.total;
+}
+
+int tdt_loss_fwd_bwd_ws(const void *logits, const int64_t sizes[4], const int64_t strides[4],
+                        int dtype, const int64_t *labels, const int64_t *logit_lens,
+                        const int64_t *label_lens, const int32_t *durations, int n_dur,
+                        int blank, double sigma, int reduction, float *loss_out, void *grad_out,
+                        void *workspace, size_t workspace_bytes, void *stream) {
+  tdt::Problem p;
+  int rc = tdt::validate(logits, sizes, strides, dtype, labels, logit_lens, label_lens,
+                         durations, n_dur, blank, sigma, reduction, loss_out, grad_out, &p);
+  if (rc != TDT_OK) return rc;
+  tdt::Layout L;
+  if (!tdt::make_layout(sizes, n_dur, &L)) return TDT_ERR_BAD_SIZES;
+  if (!workspace) return TDT_ERR_NULL_POINTER;
+  if (workspace_bytes < L.total) return TDT_ERR_WORKSPACE_TOO_SMALL;
+  if (((uintptr_t)workspace % 256) != 0) return TDT_ERR_BAD_ALIGNMENT;
+  tdt::Workspace ws = tdt::carve(L, workspace);
+  return tdt::run(p, dtype, ws, loss_out, grad_out, static_cast<cudaStream_t>(stream));
+}
+
+int tdt_loss_fwd_bwd(const void *logits, const int64_t sizes[4], const int64_t strides[4],
+                     int dtype, const int64_t *labels, const int64_t *logit_lens,
+                     const int64_t *label_lens, const int32_t *durations, int n_dur, int blank,
+                     double sigma, int reduction, float *loss_out, void *grad_out,
+                     void *stream) {
+  tdt::Problem p;
+  int rc = tdt::validate(logits, sizes, strides, dtype, labels, logit_lens, label_lens,
+                         durations, n_dur, blank, sigma, reduction, loss_out, grad_out, &p);
+  if (rc != TDT_OK) return rc;
+  tdt::Layout L;
+  if (!tdt::make_layout(sizes, n_dur, &L)) return TDT_ERR_BAD_SIZES;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void *ws_ptr = nullptr;
+  if (cudaMallocAsync(&ws_ptr, L.total, s) != cudaSuccess) return TDT_ERR_CUDA;
+  tdt::Workspace ws = tdt::carve(L, ws_ptr);
+  rc = tdt::run(p, dtype, ws, loss_out, grad_out, s);
+  if (cudaFreeAsync(ws_ptr, s) != cudaSuccess && rc == TDT_OK) rc = TDT_ERR_CUDA;
+  return rc;
+}
+
+const char *tdt_status_string(int status) {
+  switch (status) {
+    case TDT_OK: return "ok";
+    case TDT_ERR_NULL_POINTER: return "a required pointer is NULL";
+    case TDT_ERR_BAD_SIZES: return "invalid sizes (B>=0, T>=1, U+1>=1, V+D>n_dur, T+U+1<=65536)";
+    case TDT_ERR_BAD_STRIDES: return "invalid strides (strides[3] must be 1, others >= 0)";
+    case TDT_ERR_BAD_DTYPE: return "unknown dtype";
+    case TDT_ERR_BAD_DURATIONS:
+      return "invalid durations (1..32 distinct values in [0, 255])";
+    case TDT_ERR_BAD_BLANK: return "blank outside [0, V)";
+    case TDT_ERR_BAD_REDUCTION: return "unknown reduction";
+    case TDT_ERR_BAD_SIGMA: return "sigma must be finite with |sigma| <= 1024";
+    case TDT_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than tdt_loss_workspace_size";
+    case TDT_ERR_CUDA: return "a CUDA call failed";
+    case TDT_ERR_BAD_ALIGNMENT: return "a pointer is not aligned to its element size";
+    default: return "unknown status";
+  }
+}
+
+int tdt_loss_version(void) { return TDT_LOSS_VERSION; }
+
+void tdt_loss_timing_enable(int on) {
+  tdt::Timing &t = tdt::timing();
+  std::lock_guard<std::mutex> g(t.mu);
+  t.on = on != 0;
+}
+
+int tdt_loss_timing_read(double *ms_out, int64_t *count_out, int n, int reset) {
+  tdt::Timing &t = tdt::timing();
+  std::lock_guard<std::mutex> g(t.mu);
+  int rc = 0;
+  for (auto &pe : t.pending) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(pe.b) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, pe.a, pe.b) != cudaSuccess)
+      rc = TDT_ERR_CUDA;
+    t.ms[pe.id] += ms;
+    t.count[pe.id] += 1;
+    t.pool.push_back(pe.a);
+    t.pool.push_back(pe.b);
+  }
+  t.pending.clear();
+  if (n > TDT_KERNEL_COUNT) n = TDT_KERNEL_COUNT;
+  for (int i = 0; i < n; ++i) {
+    if (ms_out) ms_out[i] = t.ms[i];
+    if (count_out) count_out[i] = t.count[i];
+  }
+  if (reset)
+    for (int i = 0; i < TDT_KERNEL_COUNT; ++i) {
+      t.ms[i] = 0.0;
+      t.count[i] = 0;
+    }
+  return rc != 0 ? rc : (n < 0 ? 0 : n);
+}
+
+}  // extern "C"

@@ -1,0 +1,156 @@
+// tdt_common.cuh -- definitions shared by the TDT loss kernels (sm_103a).
+//
+// Numeric representation of the lattice.  alpha, beta, the log-likelihood
+// and the per-node arc log-weights are 64-bit fixed point with 32 fraction
+// bits ("fx": value * 2^32, rounded).  Additions of fx values are exact and
+// associative, so the long alpha/beta chains ("float64 accumulation for
+// precision on long label sequences", "tdt-loss: add TDT loss kernel",
+// kernels-community PR #882, "What's in it") carry no rounding at all; the
+// only rounding per node is one fp32 exp per incoming arc of a value <= 0 and
+// one fp32 log1p of a value in [0, 1).  GB300 runs float64 at a small
+// fraction of its fp32 rate, which is why the arithmetic per arc is integer
+// + fp32 rather than float64.  |value| < 2^30 holds because log-probs are
+// clamped at -4096, |sigma| <= 1024 and T + U + 1 <= 65536.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tdt {
+
+typedef long long fx_t;
+
+constexpr int kFracBits = 32;
+constexpr double kFxOne = 4294967296.0;                     // 2^32
+constexpr fx_t kFxNegInf = (fx_t)(-0x7fffffffffffffffLL - 1);  // -inf sentinel
+constexpr float kLogProbFloor = -4096.0f;
+// ln 2 in fx, rounded from the mathematical constant 0.693147180559945309...
+constexpr fx_t kFxLn2 = (fx_t)(0.69314718055994530942 * 4294967296.0 + 0.5);
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kFxToLog2 = (float)(1.4426950408889634 / 4294967296.0);  // fx -> log2 units
+constexpr int kMaxDurations = 32;
+constexpr int kMaxDurationValue = 255;
+
+enum DType { kF32 = 0, kF16 = 1, kBF16 = 2 };
+enum Reduction { kNone = 0, kSum = 1, kMean = 2, kMeanBatch = 3, kMeanVolume = 4 };
+
+// Everything a kernel needs to know about one call.  Passed by value.
+struct Problem {
+  const void *logits;
+  long long B, T, U1, VD, V, D;   // U1 = U + 1
+  long long s0, s1, s2;           // element strides of logits (s3 == 1)
+  const long long *labels;        // [B, U1-1]
+  const long long *logit_lens;    // [B]
+  const long long *label_lens;    // [B]
+  int dur[kMaxDurations];
+  int n_dur;
+  int max_dur;
+  int blank;
+  int reduction;
+  fx_t sigma_fx;
+  long long n_diag;               // T + U1 - 1 anti-diagonals per utterance
+};
+
+// Scratch layout (device pointers carved from one workspace block).
+struct Workspace {
+  // anti-diagonal-major tables, index ((b * n_diag + t + u) * U1 + u)
+  fx_t *wb;      // lpB - sigma
+  fx_t *wl;      // lpL - sigma (label y_{u+1}); unused at u = U_b
+  fx_t *lpd;     // [D][B * n_diag * U1] duration log-probs
+  fx_t *alpha;   // [B * n_diag * U1]
+  fx_t *beta;    // [B * n_diag * U1]
+  // node-major per-row data, index n = (b * T + t) * U1 + u
+  float *lse_tok;  // log-sum-exp of the token logits
+  float *lse_dur;  // log-sum-exp of the duration logits
+  float *frac;     // [(2 + D)][nodes]: share of beta(t,u) through blank arcs,
+                   //   label arcs, and through each duration
+  // per utterance
+  fx_t *loglik;    // [B] log-likelihood from alpha
+  double *scale;   // [B] c_b, factor of dL_b/dz in the reduced loss
+  int *usable;     // [B] 1 = lengths and labels usable
+};
+
+__host__ __device__ inline long long diag_index(const Problem &p, long long b, long long t,
+                                                long long u) {
+  return (b * p.n_diag + t + u) * p.U1 + u;
+}
+
+// ---- element access -------------------------------------------------------
+template <int DT> struct Elem;
+template <> struct Elem<kF32> {
+  typedef float T;
+  static __device__ __forceinline__ float load(const float *p) { return __ldg(p); }
+  static __device__ __forceinline__ float to_float(float v) { return v; }
+  static __device__ __forceinline__ float from_float(float v) { return v; }
+};
+template <> struct Elem<kF16> {
+  typedef __half T;
+  static __device__ __forceinline__ float load(const __half *p) { return __half2float(__ldg(p)); }
+  static __device__ __forceinline__ float to_float(__half v) { return __half2float(v); }
+  static __device__ __forceinline__ __half from_float(float v) { return __float2half_rn(v); }
+};
+template <> struct Elem<kBF16> {
+  typedef __nv_bfloat16 T;
+  static __device__ __forceinline__ float load(const __nv_bfloat16 *p) {
+    return __bfloat162float(__ldg(p));
+  }
+  static __device__ __forceinline__ float to_float(__nv_bfloat16 v) { return __bfloat162float(v); }
+  static __device__ __forceinline__ __nv_bfloat16 from_float(float v) {
+    return __float2bfloat16_rn(v);
+  }
+};
+
+// ---- arithmetic helpers -----------------------------------------------------
+// 2^x for x <= 0 (and moderate positive x) with the hardware approximation
+// (ex2.approx, ~2 ulp); large negative x flush to 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// fx value of a float (exact for |x| >= 2^-8 up to 2^30).
+__device__ __forceinline__ fx_t fx_from_float(float x) {
+  return __float2ll_rn(x * 4294967296.0f);
+}
+
+// fx value of ln(s) for s >= 1, split as e*ln2 + log1p(f - 1), s = f * 2^e,
+// f in [1, 2): the integer part is exact, the rest is one log1pf.
+__device__ __forceinline__ fx_t fx_log_ge1(float s) {
+  int e;
+  float f = frexpf(s, &e);  // s = f * 2^e, f in [0.5, 1)
+  f *= 2.0f;
+  e -= 1;
+  float lf = log1pf(f - 1.0f);
+  return (fx_t)e * kFxLn2 + fx_from_float(lf);
+}
+
+// Same value as a float, for per-row normalisers used in float arithmetic.
+__device__ __forceinline__ float log_ge1(float s) { return logf(s); }
+
+__device__ __forceinline__ float fx_to_float(fx_t v) { return __ll2float_rn(v) * (1.0f / 4294967296.0f); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---- launchers (one per translation unit) ----------------------------------
+cudaError_t launch_node_tables(const Problem &p, int dtype, const Workspace &ws,
+                               cudaStream_t stream);
+cudaError_t launch_alpha(const Problem &p, const Workspace &ws, cudaStream_t stream);
+cudaError_t launch_beta(const Problem &p, const Workspace &ws, cudaStream_t stream);
+cudaError_t launch_reduce(const Problem &p, const Workspace &ws, float *loss_out,
+                          cudaStream_t stream);
+cudaError_t launch_grad(const Problem &p, int dtype, const Workspace &ws, void *grad_out,
+                        cudaStream_t stream);
+
+}  // namespace tdt
