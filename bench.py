@@ -211,10 +211,16 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override B (smaller profiling cases; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
+    if args.batch is not None:
+        from transducer_loss_asr_gb300.workloads import scaled
+
+        w = scaled(w, B=args.batch, name="%s_b%d" % (w.name, args.batch))
     if args.impl == "reference":
         return run_reference(args, w)
 

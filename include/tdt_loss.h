@@ -124,12 +124,12 @@ int tdt_loss_fwd_bwd_ws(const void *logits, const int64_t sizes[4], const int64_
                         void *grad_out, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * Benchmark support (not needed for correctness).  Kernel ids, in launch
- * order: node tables, alpha, beta, reduction, gradient.
+ * Benchmark support (not needed for correctness).  Kernel ids: node tables,
+ * lattice (alpha and beta), (unused), reduction, gradient.
  */
 #define TDT_KERNEL_TABLES 0
-#define TDT_KERNEL_ALPHA 1
-#define TDT_KERNEL_BETA 2
+#define TDT_KERNEL_LATTICE 1
+#define TDT_KERNEL_UNUSED 2
 #define TDT_KERNEL_REDUCE 3
 #define TDT_KERNEL_GRAD 4
 #define TDT_KERNEL_COUNT 5

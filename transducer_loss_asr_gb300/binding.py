@@ -153,7 +153,7 @@ def tdt_loss_version() -> int:
     return int(lib.tdt_loss_version())
 
 
-KERNEL_NAMES = ("node_tables", "alpha", "beta", "reduce", "grad")
+KERNEL_NAMES = ("node_tables", "lattice", "unused", "reduce", "grad")
 
 
 def tdt_loss_timing_enable(on: bool) -> None:

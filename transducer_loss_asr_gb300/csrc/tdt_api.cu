@@ -1,6 +1,14 @@
 // tdt_api.cu -- the C ABI (include/tdt_loss.h): argument checks, scratch
-// layout, and the order of the kernels on the caller's stream:
-//   K1 node tables -> K2 alpha -> K3 beta -> K5 reduction -> K4 gradient.
+// layout, and the order of the kernels.
+//
+// The batch is cut into up to kChunks groups of utterances.  On the caller's
+// stream: K1 node tables for chunk 0, 1, ..., then K4 gradient for chunk 0,
+// 1, ...  On an internal high-priority stream: the alpha/beta lattice pass of
+// chunk c as soon as K1 of chunk c is done, then the reduction.  K4 of chunk
+// c waits for the lattice of chunk c.  So the latency-bound lattice passes
+// (a few SMs) run under the bandwidth-bound K1/K4 passes of other chunks
+// instead of between them.  The fork and join are CUDA events, so the whole
+// call is stream-ordered (and capturable) on the caller's stream.
 #include <math.h>
 #include <string.h>
 
@@ -167,24 +175,82 @@ cudaError_t timed(int id, cudaStream_t stream, F fn) {
   return e;
 }
 
+// ---- per-device internal stream and events -----------------------------------
+constexpr int kChunks = 4;
+
+struct DeviceRes {
+  bool ready = false;
+  cudaStream_t side = nullptr;  // high priority, for the lattice passes
+  cudaEvent_t fork = nullptr, join = nullptr;
+  cudaEvent_t tables_done[kChunks] = {}, lattice_done[kChunks] = {};
+  std::mutex mu;                // one call at a time enqueues on these events
+};
+
+DeviceRes *device_res(int dev) {
+  static std::mutex mu;
+  static std::vector<DeviceRes *> all;
+  std::lock_guard<std::mutex> g(mu);
+  if ((int)all.size() <= dev) all.resize(dev + 1, nullptr);
+  if (!all[dev]) all[dev] = new DeviceRes();  // lives until process exit
+  DeviceRes *r = all[dev];
+  if (!r->ready) {
+    int lo = 0, hi = 0;
+    if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return nullptr;
+    if (cudaStreamCreateWithPriority(&r->side, cudaStreamNonBlocking, hi) != cudaSuccess)
+      return nullptr;
+    bool ok = cudaEventCreateWithFlags(&r->fork, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&r->join, cudaEventDisableTiming) == cudaSuccess;
+    for (int c = 0; c < kChunks && ok; ++c)
+      ok = cudaEventCreateWithFlags(&r->tables_done[c], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&r->lattice_done[c], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return nullptr;
+    r->ready = true;
+  }
+  return r;
+}
+
 int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void *grad_out,
         cudaStream_t stream) {
-  if (timed(TDT_KERNEL_TABLES, stream,
-            [&] { return launch_node_tables(p, dtype, ws, stream); }) != cudaSuccess)
-    return TDT_ERR_CUDA;
-  if (timed(TDT_KERNEL_ALPHA, stream, [&] { return launch_alpha(p, ws, stream); }) !=
-      cudaSuccess)
-    return TDT_ERR_CUDA;
-  if (grad_out &&
-      timed(TDT_KERNEL_BETA, stream, [&] { return launch_beta(p, ws, stream); }) != cudaSuccess)
-    return TDT_ERR_CUDA;
-  if (timed(TDT_KERNEL_REDUCE, stream,
-            [&] { return launch_reduce(p, ws, loss_out, stream); }) != cudaSuccess)
-    return TDT_ERR_CUDA;
-  if (grad_out && timed(TDT_KERNEL_GRAD, stream, [&] {
-        return launch_grad(p, dtype, ws, grad_out, stream);
-      }) != cudaSuccess)
-    return TDT_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return TDT_ERR_CUDA;
+  DeviceRes *res = device_res(dev);
+  if (!res) return TDT_ERR_CUDA;
+  std::lock_guard<std::mutex> g(res->mu);
+  const bool with_grad = grad_out != nullptr;
+  const long long rows_per_utt = p.T * p.U1;
+  const int nchunk = (int)(p.B < kChunks ? (p.B > 0 ? p.B : 1) : kChunks);
+  auto b_lo = [&](int c) { return p.B * c / nchunk; };
+  cudaStream_t side = res->side;
+#define TDT_TRY(x) \
+  do {             \
+    if ((x) != cudaSuccess) return TDT_ERR_CUDA; \
+  } while (0)
+  TDT_TRY(cudaEventRecord(res->fork, stream));
+  TDT_TRY(cudaStreamWaitEvent(side, res->fork, 0));
+  for (int c = 0; c < nchunk; ++c) {
+    const long long b0 = b_lo(c), b1 = b_lo(c + 1);
+    TDT_TRY(timed(TDT_KERNEL_TABLES, stream, [&] {
+      return launch_node_tables(p, dtype, ws, b0 * rows_per_utt, b1 * rows_per_utt, stream);
+    }));
+    TDT_TRY(cudaEventRecord(res->tables_done[c], stream));
+    TDT_TRY(cudaStreamWaitEvent(side, res->tables_done[c], 0));
+    TDT_TRY(timed(TDT_KERNEL_LATTICE, side,
+                  [&] { return launch_lattice(p, ws, b0, b1, with_grad, side); }));
+    TDT_TRY(cudaEventRecord(res->lattice_done[c], side));
+  }
+  TDT_TRY(timed(TDT_KERNEL_REDUCE, side, [&] { return launch_reduce(p, ws, loss_out, side); }));
+  TDT_TRY(cudaEventRecord(res->join, side));
+  if (with_grad) {
+    for (int c = 0; c < nchunk; ++c) {
+      const long long b0 = b_lo(c), b1 = b_lo(c + 1);
+      TDT_TRY(cudaStreamWaitEvent(stream, res->lattice_done[c], 0));
+      TDT_TRY(timed(TDT_KERNEL_GRAD, stream, [&] {
+        return launch_grad(p, dtype, ws, grad_out, b0 * rows_per_utt, b1 * rows_per_utt, stream);
+      }));
+    }
+  }
+  TDT_TRY(cudaStreamWaitEvent(stream, res->join, 0));
+#undef TDT_TRY
   return TDT_OK;
 }
 

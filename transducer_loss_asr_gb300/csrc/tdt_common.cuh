@@ -127,9 +127,6 @@ __device__ __forceinline__ fx_t fx_log_ge1(float s) {
   return (fx_t)e * kFxLn2 + fx_from_float(lf);
 }
 
-// Same value as a float, for per-row normalisers used in float arithmetic.
-__device__ __forceinline__ float log_ge1(float s) { return logf(s); }
-
 __device__ __forceinline__ float fx_to_float(fx_t v) { return __ll2float_rn(v) * (1.0f / 4294967296.0f); }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -144,13 +141,14 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---- launchers (one per translation unit) ----------------------------------
+// Rows are flat node ids n in [n_begin, n_end); utterances b in [b_begin, b_end).
 cudaError_t launch_node_tables(const Problem &p, int dtype, const Workspace &ws,
-                               cudaStream_t stream);
-cudaError_t launch_alpha(const Problem &p, const Workspace &ws, cudaStream_t stream);
-cudaError_t launch_beta(const Problem &p, const Workspace &ws, cudaStream_t stream);
+                               long long n_begin, long long n_end, cudaStream_t stream);
+cudaError_t launch_lattice(const Problem &p, const Workspace &ws, long long b_begin,
+                           long long b_end, bool with_beta, cudaStream_t stream);
 cudaError_t launch_reduce(const Problem &p, const Workspace &ws, float *loss_out,
                           cudaStream_t stream);
 cudaError_t launch_grad(const Problem &p, int dtype, const Workspace &ws, void *grad_out,
-                        cudaStream_t stream);
+                        long long n_begin, long long n_end, cudaStream_t stream);
 
 }  // namespace tdt

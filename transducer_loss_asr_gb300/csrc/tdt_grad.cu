@@ -10,105 +10,161 @@
 // The softmaxes are recomputed from the row and the saved log-sum-exps, so
 // the row is read once more and every gradient element written once, in the
 // input dtype (round to nearest).  Rows outside a lattice are written as 0.
-#include "tdt_common.cuh"
+// One warp per row; 16-byte loads and stores when the input row and the
+// output row have the same offset from a 16-byte boundary (the contiguous
+// case), coalesced scalar accesses otherwise.
+#include "tdt_rowio.cuh"
 
 namespace tdt {
 
 namespace {
 
 constexpr int kGradThreads = 256;
-constexpr int kUnroll = 8;
+constexpr int kGradUnroll = 4;
+constexpr int kScalarUnroll = 8;
+
+template <int DT>
+__device__ __forceinline__ void zero_row(typename Elem<DT>::T *out, long long VD, int lane) {
+  typedef typename Elem<DT>::T E;
+  constexpr int N = Vec<DT>::N;
+  int head = head_elems<DT>(out);
+  if (head > VD) head = (int)VD;
+  const long long nvec = (VD - head) / N;
+  const long long tail0 = head + nvec * N;
+  const E zero = Elem<DT>::from_float(0.0f);
+  if (lane < head) out[lane] = zero;
+  if (lane < VD - tail0) out[tail0 + lane] = zero;
+  uint4 *v = reinterpret_cast<uint4 *>(out + head);
+  for (long long j = lane; j < nvec; j += 32) v[j] = make_uint4(0u, 0u, 0u, 0u);
+}
 
 template <int DT>
 __global__ void __launch_bounds__(kGradThreads)
-grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad) {
+grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, long long n_begin,
+            long long n_end) {
   typedef typename Elem<DT>::T E;
+  constexpr int N = Vec<DT>::N;
   const E *logits = static_cast<const E *>(p.logits);
   const int lane = threadIdx.x & 31;
-  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const long long n = n_begin + (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (n >= n_end) return;
   const long long nodes = p.B * p.T * p.U1;
+  const long long u = n % p.U1;
+  const long long bt = n / p.U1;
+  const long long t = bt % p.T;
+  const long long b = bt / p.T;
+  E *out = grad + n * p.VD;
+  const long long Tb = p.logit_lens[b], Ub = p.label_lens[b];
+  bool live = ws.usable[b] && t < Tb && u <= Ub && ws.loglik[b] != kFxNegInf;
+  float a = 0.0f;
+  if (live) {
+    const long long q = diag_index(p, b, t, u);
+    const fx_t al = ws.alpha[q], be = ws.beta[q];
+    if (al == kFxNegInf || be == kFxNegInf) {
+      live = false;
+    } else {
+      const float occ = fast_exp2(__ll2float_rn(al + be - ws.loglik[b]) * kFxToLog2);
+      a = (float)ws.scale[b] * occ;
+    }
+  }
+  if (!live) {
+    zero_row<DT>(out, p.VD, lane);
+    return;
+  }
+  const E *row = logits + b * p.s0 + t * p.s1 + u * p.s2;
+  const float lse2 = ws.lse_tok[n] * kLog2e;
+  const float lsed2 = ws.lse_dur[n] * kLog2e;
+  const float ab = a * ws.frac[n];           // a * fB, taken off the blank entry
+  const float al = a * ws.frac[nodes + n];   // a * fL, taken off the label entry
+  const long long y = (u < Ub) ? p.labels[b * (p.U1 - 1) + u] : -1;
+  auto g_at = [&](float x, long long k) {
+    float g = a * fast_exp2(fmaf(x, kLog2e, -lse2));
+    if (k == p.blank) g -= ab;
+    if (k == y) g -= al;
+    return g;
+  };
 
-  for (long long n = warp; n < nodes; n += nwarps) {
-    const long long u = n % p.U1;
-    const long long bt = n / p.U1;
-    const long long t = bt % p.T;
-    const long long b = bt / p.T;
-    E *out = grad + n * p.VD;
-    const long long Tb = p.logit_lens[b], Ub = p.label_lens[b];
-    bool live = ws.usable[b] && t < Tb && u <= Ub && ws.loglik[b] != kFxNegInf;
-    float a = 0.0f;
-    if (live) {
-      const long long q = diag_index(p, b, t, u);
-      const fx_t al = ws.alpha[q], be = ws.beta[q];
-      if (al == kFxNegInf || be == kFxNegInf) {
-        live = false;
-      } else {
-        const float occ = fast_exp2(__ll2float_rn(al + be - ws.loglik[b]) * kFxToLog2);
-        a = (float)ws.scale[b] * occ;
+  const uintptr_t ai = reinterpret_cast<uintptr_t>(row), ao = reinterpret_cast<uintptr_t>(out);
+  if (((ai ^ ao) & 15) == 0) {
+    int head = head_elems<DT>(row);
+    if (head > p.V) head = (int)p.V;
+    const long long nvec = (p.V - head) / N;
+    const long long tail0 = head + nvec * N;
+    const int ntail = (int)(p.V - tail0);
+    if (lane < head) out[lane] = Elem<DT>::from_float(g_at(Elem<DT>::load(row + lane), lane));
+    if (lane < ntail) {
+      const long long k = tail0 + lane;
+      out[k] = Elem<DT>::from_float(g_at(Elem<DT>::load(row + k), k));
+    }
+    const char *vin = reinterpret_cast<const char *>(row + head);
+    char *vout = reinterpret_cast<char *>(out + head);
+    // vectors holding the two special entries (or -1)
+    const long long jb = (p.blank >= head && p.blank < tail0) ? (p.blank - head) / N : -1;
+    const long long jy = (y >= head && y < tail0) ? (y - head) / N : -1;
+    for (long long j0 = 0; j0 < nvec; j0 += 32 * kGradUnroll) {
+      uint4 v[kGradUnroll];
+#pragma unroll
+      for (int k = 0; k < kGradUnroll; ++k) {
+        const long long j = j0 + k * 32 + lane;
+        if (j < nvec) v[k] = ld_vec(vin + j * 16);
+      }
+#pragma unroll
+      for (int k = 0; k < kGradUnroll; ++k) {
+        const long long j = j0 + k * 32 + lane;
+        if (j < nvec) {
+          float x[N];
+          unpack<DT>(v[k], x);
+#pragma unroll
+          for (int e = 0; e < N; ++e) x[e] = a * fast_exp2(fmaf(x[e], kLog2e, -lse2));
+          if (j == jb) x[(p.blank - head) % N] -= ab;
+          if (j == jy) x[(y - head) % N] -= al;
+          *reinterpret_cast<uint4 *>(vout + j * 16) = pack<DT>(x);
+        }
       }
     }
-    if (!live) {
-      const E zero = Elem<DT>::from_float(0.0f);
-      for (long long k = lane; k < p.VD; k += 32) out[k] = zero;
-      continue;
-    }
-    const E *row = logits + b * p.s0 + t * p.s1 + u * p.s2;
-    const float lse_t = ws.lse_tok[n];
-    const float lse_d = ws.lse_dur[n];
-    const float fb = ws.frac[n];
-    const float fl = ws.frac[nodes + n];
-    const long long y = (u < Ub) ? p.labels[b * (p.U1 - 1) + u] : -1;
-    for (long long k0 = 0; k0 < p.V; k0 += 32 * kUnroll) {
-      float x[kUnroll];
+  } else {
+    for (long long k0 = 0; k0 < p.V; k0 += 32 * kScalarUnroll) {
+      float x[kScalarUnroll];
 #pragma unroll
-      for (int j = 0; j < kUnroll; ++j) {
+      for (int j = 0; j < kScalarUnroll; ++j) {
         const long long k = k0 + j * 32 + lane;
         x[j] = (k < p.V) ? Elem<DT>::load(row + k) : 0.0f;
       }
 #pragma unroll
-      for (int j = 0; j < kUnroll; ++j) {
+      for (int j = 0; j < kScalarUnroll; ++j) {
         const long long k = k0 + j * 32 + lane;
-        if (k < p.V) {
-          float g = fast_exp2((x[j] - lse_t) * kLog2e);
-          if (k == p.blank) g -= fb;
-          if (k == y) g -= fl;
-          out[k] = Elem<DT>::from_float(a * g);
-        }
+        if (k < p.V) out[k] = Elem<DT>::from_float(g_at(x[j], k));
       }
     }
-    if (lane < p.D) {
-      const float zd = Elem<DT>::load(row + p.V + lane);
-      const float g = fast_exp2((zd - lse_d) * kLog2e) - ws.frac[(long long)(2 + lane) * nodes + n];
-      out[p.V + lane] = Elem<DT>::from_float(a * g);
-    }
+  }
+  if (lane < p.D) {
+    const float zd = Elem<DT>::load(row + p.V + lane);
+    const float g = fast_exp2(fmaf(zd, kLog2e, -lsed2)) - ws.frac[(long long)(2 + lane) * nodes + n];
+    out[p.V + lane] = Elem<DT>::from_float(a * g);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_grad(const Problem &p, int dtype, const Workspace &ws, void *grad_out,
-                        cudaStream_t stream) {
-  const long long nodes = p.B * p.T * p.U1;
-  if (nodes == 0) return cudaSuccess;
-  int dev = 0, sms = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+                        long long n_begin, long long n_end, cudaStream_t stream) {
+  const long long rows = n_end - n_begin;
+  if (rows <= 0) return cudaSuccess;
   const long long warps_per_block = kGradThreads / 32;
-  long long blocks = (nodes + warps_per_block - 1) / warps_per_block;
-  const long long cap = (long long)sms * 8;
-  if (blocks > cap) blocks = cap;
+  const long long blocks = (rows + warps_per_block - 1) / warps_per_block;
   dim3 grid((unsigned)blocks), block(kGradThreads);
   switch (dtype) {
     case kF32:
-      grad_kernel<kF32><<<grid, block, 0, stream>>>(p, ws, static_cast<float *>(grad_out));
+      grad_kernel<kF32><<<grid, block, 0, stream>>>(p, ws, static_cast<float *>(grad_out),
+                                                    n_begin, n_end);
       break;
     case kF16:
-      grad_kernel<kF16><<<grid, block, 0, stream>>>(p, ws, static_cast<__half *>(grad_out));
+      grad_kernel<kF16><<<grid, block, 0, stream>>>(p, ws, static_cast<__half *>(grad_out),
+                                                    n_begin, n_end);
       break;
     default:
-      grad_kernel<kBF16><<<grid, block, 0, stream>>>(p, ws,
-                                                     static_cast<__nv_bfloat16 *>(grad_out));
+      grad_kernel<kBF16><<<grid, block, 0, stream>>>(
+          p, ws, static_cast<__nv_bfloat16 *>(grad_out), n_begin, n_end);
       break;
   }
   return cudaGetLastError();

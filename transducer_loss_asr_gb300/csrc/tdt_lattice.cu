@@ -51,8 +51,34 @@ __device__ __forceinline__ fx_t lpd_at(const Problem &p, const Workspace &ws, in
   return ws.lpd[(long long)i * (p.B * p.n_diag * p.U1) + q];
 }
 
-__global__ void __launch_bounds__(kLatticeMaxThreads) alpha_kernel(Problem p, Workspace ws) {
-  const long long b = blockIdx.x;
+// log-likelihood: a blank arc from (T_b - d, U_b) lands exactly on T_b.
+// Reads alpha and the tables from global memory (one thread).
+__device__ fx_t termination(const Problem &p, const Workspace &ws, long long b, long long Tb,
+                            long long Ub) {
+  fx_t m = kFxNegInf;
+  for (int i = 0; i < p.n_dur; ++i) {
+    const int d = p.dur[i];
+    if (d <= 0 || Tb - d < 0) continue;
+    const long long q = diag_index(p, b, Tb - d, Ub);
+    const fx_t a = ws.alpha[q];
+    if (a != kFxNegInf) m = fmax_fx(m, a + ws.wb[q] + lpd_at(p, ws, i, q));
+  }
+  if (m == kFxNegInf) return kFxNegInf;
+  float sum = 0.0f;
+  for (int i = 0; i < p.n_dur; ++i) {
+    const int d = p.dur[i];
+    if (d <= 0 || Tb - d < 0) continue;
+    const long long q = diag_index(p, b, Tb - d, Ub);
+    const fx_t a = ws.alpha[q];
+    if (a != kFxNegInf)
+      sum += fast_exp2(__ll2float_rn(a + ws.wb[q] + lpd_at(p, ws, i, q) - m) * kFxToLog2);
+  }
+  return m + fx_log_ge1(sum);
+}
+
+__global__ void __launch_bounds__(kLatticeMaxThreads)
+alpha_kernel(Problem p, Workspace ws, long long b0) {
+  const long long b = b0 + blockIdx.x;
   double sum_u;
   const bool ok = check_utterance(p, b, &sum_u);
   if (threadIdx.x == 0) {
@@ -117,38 +143,15 @@ __global__ void __launch_bounds__(kLatticeMaxThreads) alpha_kernel(Problem p, Wo
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    // termination: a blank arc from (T_b - d, U_b) lands exactly on T_b
-    fx_t m = kFxNegInf;
-    for (int i = 0; i < p.n_dur; ++i) {
-      const int d = p.dur[i];
-      if (d <= 0 || Tb - d < 0) continue;
-      const long long q = diag_index(p, b, Tb - d, Ub);
-      const fx_t a = ws.alpha[q];
-      if (a != kFxNegInf) m = fmax_fx(m, a + ws.wb[q] + lpd_at(p, ws, i, q));
-    }
-    fx_t ll = kFxNegInf;
-    if (m != kFxNegInf) {
-      float sum = 0.0f;
-      for (int i = 0; i < p.n_dur; ++i) {
-        const int d = p.dur[i];
-        if (d <= 0 || Tb - d < 0) continue;
-        const long long q = diag_index(p, b, Tb - d, Ub);
-        const fx_t a = ws.alpha[q];
-        if (a != kFxNegInf)
-          sum += fast_exp2(__ll2float_rn(a + ws.wb[q] + lpd_at(p, ws, i, q) - m) * kFxToLog2);
-      }
-      ll = m + fx_log_ge1(sum);
-    }
-    ws.loglik[b] = ll;
-  }
+  if (threadIdx.x == 0) ws.loglik[b] = termination(p, ws, b, Tb, Ub);
 }
 
 // beta(t,u) over the outgoing arcs of (t,u); also the share of beta(t,u)
 // that goes through blank arcs, label arcs, and each duration (the arc
 // posteriors divided by the node occupancy), for the gradient pass.
-__global__ void __launch_bounds__(kLatticeMaxThreads) beta_kernel(Problem p, Workspace ws) {
-  const long long b = blockIdx.x;
+__global__ void __launch_bounds__(kLatticeMaxThreads)
+beta_kernel(Problem p, Workspace ws, long long b0) {
+  const long long b = b0 + blockIdx.x;
   double sum_u;
   const bool ok = check_utterance(p, b, &sum_u);
   if (!ok) return;
@@ -254,17 +257,252 @@ int lattice_threads(const Problem &p) {
   return (int)th;
 }
 
-}  // namespace
+// ---------------------------------------------------------------------------
+// Shared-memory variant (U+1 <= 1024 and the rings fit in shared memory):
+// thread u owns lattice row u.  alpha (or beta) of the last RA diagonals sits
+// in a shared ring, and the per-node tables of the diagonals in flight in a
+// second ring that cp.async fills kPrefetch diagonals ahead, so no global
+// round trip sits on the step-to-step critical path.  blockIdx.y = 0 runs
+// alpha, 1 runs beta (independent given the tables).
 
-cudaError_t launch_alpha(const Problem &p, const Workspace &ws, cudaStream_t stream) {
-  if (p.B == 0) return cudaSuccess;
-  alpha_kernel<<<(unsigned)p.B, lattice_threads(p), 0, stream>>>(p, ws);
-  return cudaGetLastError();
+constexpr int kPrefetch = 6;
+
+__device__ __forceinline__ void cp_async8(void *smem, const void *gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(sa), "l"(gmem));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-cudaError_t launch_beta(const Problem &p, const Workspace &ws, cudaStream_t stream) {
-  if (p.B == 0) return cudaSuccess;
-  beta_kernel<<<(unsigned)p.B, lattice_threads(p), 0, stream>>>(p, ws);
+struct Rings {
+  fx_t *A;      // [RA][U1p]
+  fx_t *W;      // [RW][F][U1p]: F = 2 + D fields (wb, wl, lpd[0..D-1])
+  int mA, mW;   // RA - 1, RW - 1 (powers of two)
+  int U1p, F;
+  __device__ fx_t &a(long long q, int u) const { return A[(q & mA) * U1p + u]; }
+  __device__ fx_t &w(long long q, int f, int u) const {
+    return W[((q & mW) * F + f) * (long long)U1p + u];
+  }
+};
+
+// Start the copies of diagonal q's table entries for this thread's node.
+__device__ __forceinline__ void prefetch_diag(const Problem &p, const Workspace &ws,
+                                              const Rings &r, long long b, long long q,
+                                              long long Tb, long long Ub, int u) {
+  const long long t = q - u;
+  if (q >= 0 && u <= Ub && t >= 0 && t < Tb) {
+    const long long gi = diag_index(p, b, t, u);
+    const long long stride = p.B * p.n_diag * p.U1;
+    cp_async8(&r.w(q, 0, u), ws.wb + gi);
+    cp_async8(&r.w(q, 1, u), ws.wl + gi);
+    for (int i = 0; i < p.n_dur; ++i) cp_async8(&r.w(q, 2 + i, u), ws.lpd + i * stride + gi);
+  }
+  cp_async_commit();
+}
+
+template <int MAXD>
+__device__ void alpha_smem(const Problem &p, const Workspace &ws, const Rings &r, long long b,
+                           long long Tb, long long Ub) {
+  const int u = threadIdx.x;
+  const long long nsteps = Tb + Ub;
+  for (int k = 0; k < kPrefetch; ++k) prefetch_diag(p, ws, r, b, k, Tb, Ub, u);
+  for (long long s = 0; s < nsteps; ++s) {
+    prefetch_diag(p, ws, r, b, s + kPrefetch, Tb, Ub, u);
+    cp_async_wait<kPrefetch>();
+    __syncthreads();
+    const long long t = s - u;
+    if (u <= Ub && t >= 0 && t < Tb) {
+      fx_t val = 0;
+      if (s > 0) {
+        fx_t c[2 * MAXD];
+#pragma unroll
+        for (int i = 0; i < MAXD; ++i) {
+          fx_t cb = kFxNegInf, cl = kFxNegInf;
+          if (i < p.n_dur) {
+            const int d = p.dur[i];
+            if (t - d >= 0) {
+              if (d > 0) {
+                const fx_t a = r.a(s - d, u);
+                if (a != kFxNegInf) cb = a + r.w(s - d, 0, u) + r.w(s - d, 2 + i, u);
+              }
+              if (u >= 1) {
+                const fx_t a = r.a(s - d - 1, u - 1);
+                if (a != kFxNegInf) cl = a + r.w(s - d - 1, 1, u - 1) + r.w(s - d - 1, 2 + i, u - 1);
+              }
+            }
+          }
+          c[2 * i] = cb;
+          c[2 * i + 1] = cl;
+        }
+        fx_t m = c[0];
+#pragma unroll
+        for (int k = 1; k < 2 * MAXD; ++k) m = fmax_fx(m, c[k]);
+        if (m == kFxNegInf) {
+          val = kFxNegInf;
+        } else {
+          float sum = 0.0f;
+#pragma unroll
+          for (int k = 0; k < 2 * MAXD; ++k)
+            if (c[k] != kFxNegInf) sum += fast_exp2(__ll2float_rn(c[k] - m) * kFxToLog2);
+          val = m + fx_log_ge1(sum);
+        }
+      }
+      r.a(s, u) = val;
+      ws.alpha[diag_index(p, b, t, u)] = val;
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+}
+
+template <int MAXD>
+__device__ void beta_smem(const Problem &p, const Workspace &ws, const Rings &r, long long b,
+                          long long Tb, long long Ub) {
+  const int u = threadIdx.x;
+  const long long last = Tb + Ub - 1;
+  const long long nodes = p.B * p.T * p.U1;
+  for (int k = 0; k < kPrefetch; ++k) prefetch_diag(p, ws, r, b, last - k, Tb, Ub, u);
+  for (long long q = last; q >= 0; --q) {
+    prefetch_diag(p, ws, r, b, q - kPrefetch, Tb, Ub, u);
+    cp_async_wait<kPrefetch>();
+    __syncthreads();
+    const long long t = q - u;
+    if (u <= Ub && t >= 0 && t < Tb) {
+      const fx_t wb = r.w(q, 0, u), wl = r.w(q, 1, u);
+      fx_t cb[MAXD], cl[MAXD];
+#pragma unroll
+      for (int i = 0; i < MAXD; ++i) {
+        cb[i] = kFxNegInf;
+        cl[i] = kFxNegInf;
+        if (i < p.n_dur) {
+          const int d = p.dur[i];
+          const fx_t ld = r.w(q, 2 + i, u);
+          if (d > 0) {
+            if (t + d < Tb) {
+              const fx_t bb = r.a(q + d, u);
+              if (bb != kFxNegInf) cb[i] = bb + wb + ld;
+            } else if (t + d == Tb && u == Ub) {
+              cb[i] = wb + ld;
+            }
+          }
+          if (u < Ub && t + d < Tb) {
+            const fx_t bb = r.a(q + d + 1, u + 1);
+            if (bb != kFxNegInf) cl[i] = bb + wl + ld;
+          }
+        }
+      }
+      fx_t m = kFxNegInf;
+#pragma unroll
+      for (int i = 0; i < MAXD; ++i) m = fmax_fx(m, fmax_fx(cb[i], cl[i]));
+      const long long n = (b * p.T + t) * p.U1 + u;
+      fx_t val = kFxNegInf;
+      if (m == kFxNegInf) {
+        for (int k = 0; k < 2 + p.n_dur; ++k) ws.frac[(long long)k * nodes + n] = 0.0f;
+      } else {
+        float eb[MAXD], el[MAXD], sb = 0.0f, sl = 0.0f;
+#pragma unroll
+        for (int i = 0; i < MAXD; ++i) {
+          eb[i] = cb[i] != kFxNegInf ? fast_exp2(__ll2float_rn(cb[i] - m) * kFxToLog2) : 0.0f;
+          el[i] = cl[i] != kFxNegInf ? fast_exp2(__ll2float_rn(cl[i] - m) * kFxToLog2) : 0.0f;
+          sb += eb[i];
+          sl += el[i];
+        }
+        const float tot = sb + sl;
+        const float inv = 1.0f / tot;
+        ws.frac[n] = sb * inv;
+        ws.frac[nodes + n] = sl * inv;
+#pragma unroll
+        for (int i = 0; i < MAXD; ++i)
+          if (i < p.n_dur) ws.frac[(long long)(2 + i) * nodes + n] = (eb[i] + el[i]) * inv;
+        val = m + fx_log_ge1(tot);
+      }
+      r.a(q, u) = val;
+      ws.beta[diag_index(p, b, t, u)] = val;
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+}
+
+template <int MAXD>
+__global__ void __launch_bounds__(kLatticeMaxThreads)
+lattice_smem_kernel(Problem p, Workspace ws, long long b0, int RA, int RW) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const long long b = b0 + blockIdx.x;
+  const bool is_beta = blockIdx.y == 1;
+  double sum_u;
+  const bool ok = check_utterance(p, b, &sum_u);
+  if (!is_beta && threadIdx.x == 0) {
+    ws.usable[b] = ok ? 1 : 0;
+    double c = 1.0;
+    if (p.reduction == kMean) c = 1.0 / ((double)p.B * (double)p.label_lens[b]);
+    else if (p.reduction == kMeanBatch) c = 1.0 / (double)p.B;
+    else if (p.reduction == kMeanVolume) c = 1.0 / sum_u;
+    ws.scale[b] = c;
+    if (!ok) ws.loglik[b] = kFxNegInf;
+  }
+  if (!ok) return;
+  Rings r;
+  r.U1p = blockDim.x;
+  r.F = 2 + p.n_dur;
+  r.mA = RA - 1;
+  r.mW = RW - 1;
+  r.A = reinterpret_cast<fx_t *>(smem_raw);
+  r.W = r.A + (long long)RA * r.U1p;
+  const long long Tb = p.logit_lens[b], Ub = p.label_lens[b];
+  if (!is_beta) {
+    alpha_smem<MAXD>(p, ws, r, b, Tb, Ub);
+    if (threadIdx.x == 0) ws.loglik[b] = termination(p, ws, b, Tb, Ub);
+  } else {
+    beta_smem<MAXD>(p, ws, r, b, Tb, Ub);
+  }
+}
+
+int pow2_at_least(int v) {
+  int r = 1;
+  while (r < v) r <<= 1;
+  return r;
+}
+
+// Shared bytes of the ring variant, or 0 when it does not apply.
+size_t smem_plan(const Problem &p, int *RA, int *RW, int *threads) {
+  if (p.U1 > kLatticeMaxThreads || p.n_dur > 16) return 0;
+  const int th = lattice_threads(p);
+  const int ra = pow2_at_least(p.max_dur + 2);
+  const int rw = pow2_at_least(kPrefetch + p.max_dur + 3);
+  const size_t bytes = ((size_t)ra + (size_t)rw * (size_t)(2 + p.n_dur)) * (size_t)th * 8;
+  if (bytes > 200 * 1024) return 0;
+  *RA = ra;
+  *RW = rw;
+  *threads = th;
+  return bytes;
+}
+
+}  // namespace
+
+cudaError_t launch_lattice(const Problem &p, const Workspace &ws, long long b_begin,
+                           long long b_end, bool with_beta, cudaStream_t stream) {
+  const long long nb = b_end - b_begin;
+  if (nb <= 0) return cudaSuccess;
+  int RA = 0, RW = 0, th = 0;
+  const size_t bytes = smem_plan(p, &RA, &RW, &th);
+  if (bytes > 0) {
+    dim3 grid((unsigned)nb, with_beta ? 2u : 1u);
+    if (p.n_dur <= 8) {
+      cudaFuncSetAttribute(lattice_smem_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)bytes);
+      lattice_smem_kernel<8><<<grid, th, bytes, stream>>>(p, ws, b_begin, RA, RW);
+    } else {
+      cudaFuncSetAttribute(lattice_smem_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)bytes);
+      lattice_smem_kernel<16><<<grid, th, bytes, stream>>>(p, ws, b_begin, RA, RW);
+    }
+    return cudaGetLastError();
+  }
+  alpha_kernel<<<(unsigned)nb, lattice_threads(p), 0, stream>>>(p, ws, b_begin);
+  if (with_beta) beta_kernel<<<(unsigned)nb, lattice_threads(p), 0, stream>>>(p, ws, b_begin);
   return cudaGetLastError();
 }
 

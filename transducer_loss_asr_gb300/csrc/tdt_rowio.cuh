@@ -1,0 +1,81 @@
+// tdt_rowio.cuh -- 16-byte vector access to one logits / gradient row.
+//
+// A row of V+D elements may start at any element-aligned address (rows of
+// [..., 8198] fp32 are 8-byte aligned, a bf16 slice of a [..., 8205] tensor
+// only 2-byte aligned), so a warp walks a row as: a scalar head up to the
+// first 16-byte boundary, a body of 16-byte vectors, a scalar tail.  This
+// keeps every body load a full 16-byte access whatever the row stride is
+// ("Vectorized Memory Access", "cuda-kernels" skill page, re-derived for
+// rows that are not 16-byte aligned).
+#pragma once
+
+#include "tdt_common.cuh"
+
+namespace tdt {
+
+template <int DT> struct Vec {
+  static constexpr int N = 16 / (int)sizeof(typename Elem<DT>::T);  // elements per vector
+};
+
+// Streaming 16-byte load through the read-only path.
+__device__ __forceinline__ uint4 ld_vec(const void *p) {
+  return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+template <int DT> __device__ __forceinline__ void unpack(uint4 v, float *x);
+template <> __device__ __forceinline__ void unpack<kF32>(uint4 v, float *x) {
+  x[0] = __uint_as_float(v.x);
+  x[1] = __uint_as_float(v.y);
+  x[2] = __uint_as_float(v.z);
+  x[3] = __uint_as_float(v.w);
+}
+template <> __device__ __forceinline__ void unpack<kBF16>(uint4 v, float *x) {
+  const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+template <> __device__ __forceinline__ void unpack<kF16>(uint4 v, float *x) {
+  const unsigned w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+    float2 f = __half22float2(h);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+}
+
+template <int DT> __device__ __forceinline__ uint4 pack(const float *x);
+template <> __device__ __forceinline__ uint4 pack<kF32>(const float *x) {
+  return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                    __float_as_uint(x[3]));
+}
+template <> __device__ __forceinline__ uint4 pack<kBF16>(const float *x) {
+  unsigned w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+    w[i] = *reinterpret_cast<unsigned *>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+template <> __device__ __forceinline__ uint4 pack<kF16>(const float *x) {
+  unsigned w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 h = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+    w[i] = *reinterpret_cast<unsigned *>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Elements before the first 16-byte boundary of a row starting at p.
+template <int DT> __device__ __forceinline__ int head_elems(const void *p) {
+  const int mis = (int)(reinterpret_cast<uintptr_t>(p) & 15);
+  return ((16 - mis) & 15) / (int)sizeof(typename Elem<DT>::T);
+}
+
+}  // namespace tdt

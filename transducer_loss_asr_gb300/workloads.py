@@ -14,8 +14,10 @@ Recipe (all integers uniform and inclusive; "N(0, s)" has standard deviation s):
             then cast to the workload dtype (the cast tensor is the input);
             a ``base_vd`` wider than V+D makes the input the view
             ``base[..., :V+D]``
-  labels  = uniform in [0, blank-1] (blank = V-1 in every workload), entries
-            at u >= U_b set to -100
+  labels  = uniform over the V-1 tokens other than blank (drawn in [0, V-2],
+            values >= blank shifted up by one; blank = V-1 in every named
+            workload, where this is uniform in [0, blank-1]), entries at
+            u >= U_b set to -100
   T_b, U_b = full, or uniform in the stated ranges
 Integers come from a CPU generator seeded with ``seed + 1`` so that they do
 not depend on the device.
@@ -124,7 +126,8 @@ def make_inputs(w: Workload | str, device="cpu", seed: int | None = None):
         label_lens = torch.full((w.B,), w.U, dtype=torch.int64)
     else:
         label_lens = torch.randint(w.U_range[0], w.U_range[1] + 1, (w.B,), generator=ig)
-    labels = torch.randint(0, w.blank, (w.B, max(w.U, 0)), generator=ig, dtype=torch.int64)
+    labels = torch.randint(0, w.V - 1, (w.B, max(w.U, 0)), generator=ig, dtype=torch.int64)
+    labels = labels + (labels >= w.blank).to(torch.int64)
     if w.U > 0:
         pad = torch.arange(w.U)[None, :] >= label_lens[:, None]
         labels = labels.masked_fill(pad, -100)
