@@ -93,6 +93,7 @@ extern "C" {
 #define TDT_ERR_WORKSPACE_TOO_SMALL (-9)
 #define TDT_ERR_CUDA (-10)
 #define TDT_ERR_BAD_ALIGNMENT (-11)
+#define TDT_ERR_NOALLOC_TOO_LARGE (-12)
 
 /*
  * Loss and gradient in one call.  Internal scratch (per-node tables, alpha,
@@ -122,6 +123,33 @@ int tdt_loss_fwd_bwd_ws(const void *logits, const int64_t sizes[4], const int64_
                         const int64_t *label_lens, const int32_t *durations, int n_dur,
                         int blank, double sigma, int reduction, float *loss_out,
                         void *grad_out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Same loss and gradient as tdt_loss_fwd_bwd for callers that cannot
+ * allocate device memory (the pages have no counterpart: this is an addition
+ * of this library).  Some callers may not call cudaMalloc or any allocator:
+ * code running while another component owns the device memory pool, or
+ * runtimes that reserve all memory at start-up and treat a later
+ * allocation as an error.  This entry point allocates nothing: its scratch
+ * is a fixed device array of TDT_NOALLOC_MAX_WORKSPACE_BYTES inside the
+ * library, held on every device that loads the library until the process
+ * exits.  The caller still passes every input and output buffer.
+ *   - Problems whose tdt_loss_workspace_size exceeds the array are rejected
+ *     with TDT_ERR_NOALLOC_TOO_LARGE before anything is enqueued.
+ *   - All calls on a device share the array: calls whose GPU work overlaps
+ *     (other streams, unordered host threads) race.  Order them on one
+ *     stream.  No entry of the array has to start at zero.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - The kernels run one after another on `stream`; no internal stream or
+ *     event is created.
+ */
+#define TDT_NOALLOC_MAX_WORKSPACE_BYTES (64u * 1024u * 1024u)
+int tdt_loss_fwd_bwd_noalloc(const void *logits, const int64_t sizes[4],
+                             const int64_t strides[4], int dtype, const int64_t *labels,
+                             const int64_t *logit_lens, const int64_t *label_lens,
+                             const int32_t *durations, int n_dur, int blank, double sigma,
+                             int reduction, float *loss_out, void *grad_out, void *stream);
 
 /*
  * Benchmark support (not needed for correctness).  Kernel ids: node tables,

@@ -42,6 +42,8 @@ def _load() -> ctypes.CDLL:
     lib.tdt_loss_fwd_bwd.argtypes = common + [P]
     lib.tdt_loss_fwd_bwd_ws.restype = I
     lib.tdt_loss_fwd_bwd_ws.argtypes = common + [P, ctypes.c_size_t, P]
+    lib.tdt_loss_fwd_bwd_noalloc.restype = I
+    lib.tdt_loss_fwd_bwd_noalloc.argtypes = common + [P]
     lib.tdt_loss_workspace_size.restype = ctypes.c_size_t
     lib.tdt_loss_workspace_size.argtypes = [P, I]
     lib.tdt_status_string.restype = ctypes.c_char_p
@@ -137,6 +139,28 @@ def tdt_loss_fwd_bwd_ws(logits, labels, logit_lens, label_lens, durations, blank
     with torch.cuda.device(logits.device):
         _check(lib.tdt_loss_fwd_bwd_ws(*args, _ptr(workspace), workspace.numel(),
                                        _stream_handle(logits.device)))
+    return loss_out, grad_out
+
+
+NOALLOC_MAX_WORKSPACE_BYTES = 64 * 1024 * 1024
+
+
+def tdt_loss_fwd_bwd_noalloc(logits, labels, logit_lens, label_lens, durations, blank,
+                             sigma=0.0, reduction="mean_volume", loss_out=None, grad_out=None,
+                             compute_grad=True):
+    """As tdt_loss_fwd_bwd, for callers that cannot allocate device memory.
+
+    The library allocates nothing: its scratch is a fixed 64 MiB device array
+    inside the library (problems needing more are rejected); every call on a
+    device shares it, so order the calls on one stream.  Only the outputs
+    are created here when not given -- pass loss_out and grad_out to
+    allocate nothing at all.
+    """
+    args, loss_out, grad_out = _marshal(logits, labels, logit_lens, label_lens, durations,
+                                        blank, sigma, reduction, loss_out, grad_out,
+                                        compute_grad)
+    with torch.cuda.device(logits.device):
+        _check(lib.tdt_loss_fwd_bwd_noalloc(*args, _stream_handle(logits.device)))
     return loss_out, grad_out
 
 

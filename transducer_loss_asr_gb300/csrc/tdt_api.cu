@@ -23,9 +23,7 @@ namespace {
 
 size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
 
-struct Layout {
-  size_t wb, wl, lpd, alpha, beta, lse_tok, lse_dur, frac, loglik, scale, usable, total;
-};
+}  // namespace
 
 bool make_layout(const int64_t sizes[4], int n_dur, Layout *L) {
   if (!sizes) return false;
@@ -125,6 +123,8 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
   p->n_diag = T + U1 - 1;
   return TDT_OK;
 }
+
+namespace {
 
 // ---- optional per-kernel timing (benchmarks) --------------------------------
 struct Timing {
@@ -318,6 +318,9 @@ const char *tdt_status_string(int status) {
     case TDT_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than tdt_loss_workspace_size";
     case TDT_ERR_CUDA: return "a CUDA call failed";
     case TDT_ERR_BAD_ALIGNMENT: return "a pointer is not aligned to its element size";
+    case TDT_ERR_NOALLOC_TOO_LARGE:
+      return "problem needs more scratch than the fixed array of tdt_loss_fwd_bwd_noalloc "
+             "(TDT_NOALLOC_MAX_WORKSPACE_BYTES); use tdt_loss_fwd_bwd or tdt_loss_fwd_bwd_ws";
     default: return "unknown status";
   }
 }

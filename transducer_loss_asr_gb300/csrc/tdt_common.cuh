@@ -140,6 +140,17 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// ---- host side shared by the entry points (tdt_api.cu) ----------------------
+struct Layout {  // byte offsets of the scratch regions inside one block
+  size_t wb, wl, lpd, alpha, beta, lse_tok, lse_dur, frac, loglik, scale, usable, total;
+};
+bool make_layout(const int64_t sizes[4], int n_dur, Layout *L);
+Workspace carve(const Layout &L, void *base);
+int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4], int dtype,
+             const int64_t *labels, const int64_t *logit_lens, const int64_t *label_lens,
+             const int32_t *durations, int n_dur, int blank, double sigma, int reduction,
+             const float *loss_out, const void *grad_out, Problem *p);
+
 // ---- launchers (one per translation unit) ----------------------------------
 // Rows are flat node ids n in [n_begin, n_end); utterances b in [b_begin, b_end).
 cudaError_t launch_node_tables(const Problem &p, int dtype, const Workspace &ws,
