@@ -3,9 +3,10 @@
 //
 // The batch is cut into up to kChunks groups of utterances.  On the caller's
 // stream: K1 node tables for chunk 0, 1, ..., then K4 gradient for chunk 0,
-// 1, ...  On an internal high-priority stream: the alpha/beta lattice pass of
-// chunk c as soon as K1 of chunk c is done, then the reduction.  K4 of chunk
-// c waits for the lattice of chunk c.  So the latency-bound lattice passes
+// 1, ...  On internal high-priority streams (one per chunk): the alpha/beta
+// lattice pass of chunk c as soon as K1 of chunk c is done; then the
+// reduction once every chunk's lattice is done.  K4 of chunk c waits for the
+// lattice of chunk c.  So the latency-bound lattice passes
 // (a few SMs) run under the bandwidth-bound K1/K4 passes of other chunks
 // instead of between them.  The fork and join are CUDA events, so the whole
 // call is stream-ordered (and capturable) on the caller's stream.
@@ -38,15 +39,13 @@ bool make_layout(const int64_t sizes[4], int n_dur, Layout *L) {
     off = align_up(off + bytes);
     return at;
   };
-  L->wb = take(ndiag * 8);
-  L->wl = take(ndiag * 8);
-  L->lpd = take(ndiag * 8 * (size_t)n_dur);
-  L->alpha = take(ndiag * 8);
-  L->beta = take(ndiag * 8);
+  L->arcw = take(ndiag * 8 * 2 * (size_t)n_dur);
+  L->alpha = take(ndiag * sizeof(LV));
+  L->beta = take(ndiag * sizeof(LV));
   L->lse_tok = take(nodes * 4);
   L->lse_dur = take(nodes * 4);
   L->frac = take(nodes * 4 * (size_t)(2 + n_dur));
-  L->loglik = take((size_t)B * 8);
+  L->loglik = take((size_t)B * sizeof(LV));
   L->scale = take((size_t)B * 8);
   L->usable = take((size_t)B * 4);
   L->total = off > 0 ? off : 256;
@@ -56,15 +55,13 @@ bool make_layout(const int64_t sizes[4], int n_dur, Layout *L) {
 Workspace carve(const Layout &L, void *base) {
   char *c = static_cast<char *>(base);
   Workspace w;
-  w.wb = reinterpret_cast<fx_t *>(c + L.wb);
-  w.wl = reinterpret_cast<fx_t *>(c + L.wl);
-  w.lpd = reinterpret_cast<fx_t *>(c + L.lpd);
-  w.alpha = reinterpret_cast<fx_t *>(c + L.alpha);
-  w.beta = reinterpret_cast<fx_t *>(c + L.beta);
+  w.arcw = reinterpret_cast<fx_t *>(c + L.arcw);
+  w.alpha = reinterpret_cast<LV *>(c + L.alpha);
+  w.beta = reinterpret_cast<LV *>(c + L.beta);
   w.lse_tok = reinterpret_cast<float *>(c + L.lse_tok);
   w.lse_dur = reinterpret_cast<float *>(c + L.lse_dur);
   w.frac = reinterpret_cast<float *>(c + L.frac);
-  w.loglik = reinterpret_cast<fx_t *>(c + L.loglik);
+  w.loglik = reinterpret_cast<LV *>(c + L.loglik);
   w.scale = reinterpret_cast<double *>(c + L.scale);
   w.usable = reinterpret_cast<int *>(c + L.usable);
   return w;
@@ -180,7 +177,7 @@ constexpr int kChunks = 4;
 
 struct DeviceRes {
   bool ready = false;
-  cudaStream_t side = nullptr;  // high priority, for the lattice passes
+  cudaStream_t side[kChunks] = {};  // high priority, one per chunk's lattice pass
   cudaEvent_t fork = nullptr, join = nullptr;
   cudaEvent_t tables_done[kChunks] = {}, lattice_done[kChunks] = {};
   std::mutex mu;                // one call at a time enqueues on these events
@@ -196,8 +193,9 @@ DeviceRes *device_res(int dev) {
   if (!r->ready) {
     int lo = 0, hi = 0;
     if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return nullptr;
-    if (cudaStreamCreateWithPriority(&r->side, cudaStreamNonBlocking, hi) != cudaSuccess)
-      return nullptr;
+    for (int c = 0; c < kChunks; ++c)
+      if (cudaStreamCreateWithPriority(&r->side[c], cudaStreamNonBlocking, hi) != cudaSuccess)
+        return nullptr;
     bool ok = cudaEventCreateWithFlags(&r->fork, cudaEventDisableTiming) == cudaSuccess &&
               cudaEventCreateWithFlags(&r->join, cudaEventDisableTiming) == cudaSuccess;
     for (int c = 0; c < kChunks && ok; ++c)
@@ -220,15 +218,15 @@ int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void 
   const long long rows_per_utt = p.T * p.U1;
   const int nchunk = (int)(p.B < kChunks ? (p.B > 0 ? p.B : 1) : kChunks);
   auto b_lo = [&](int c) { return p.B * c / nchunk; };
-  cudaStream_t side = res->side;
 #define TDT_TRY(x) \
   do {             \
     if ((x) != cudaSuccess) return TDT_ERR_CUDA; \
   } while (0)
   TDT_TRY(cudaEventRecord(res->fork, stream));
-  TDT_TRY(cudaStreamWaitEvent(side, res->fork, 0));
+  for (int c = 0; c < nchunk; ++c) TDT_TRY(cudaStreamWaitEvent(res->side[c], res->fork, 0));
   for (int c = 0; c < nchunk; ++c) {
     const long long b0 = b_lo(c), b1 = b_lo(c + 1);
+    cudaStream_t side = res->side[c];
     TDT_TRY(timed(TDT_KERNEL_TABLES, stream, [&] {
       return launch_node_tables(p, dtype, ws, b0 * rows_per_utt, b1 * rows_per_utt, stream);
     }));
@@ -238,8 +236,11 @@ int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void 
                   [&] { return launch_lattice(p, ws, b0, b1, with_grad, side); }));
     TDT_TRY(cudaEventRecord(res->lattice_done[c], side));
   }
-  TDT_TRY(timed(TDT_KERNEL_REDUCE, side, [&] { return launch_reduce(p, ws, loss_out, side); }));
-  TDT_TRY(cudaEventRecord(res->join, side));
+  // the reduction needs every chunk's log-likelihood; it joins all side streams
+  cudaStream_t side0 = res->side[0];
+  for (int c = 1; c < nchunk; ++c) TDT_TRY(cudaStreamWaitEvent(side0, res->lattice_done[c], 0));
+  TDT_TRY(timed(TDT_KERNEL_REDUCE, side0, [&] { return launch_reduce(p, ws, loss_out, side0); }));
+  TDT_TRY(cudaEventRecord(res->join, side0));
   if (with_grad) {
     for (int c = 0; c < nchunk; ++c) {
       const long long b0 = b_lo(c), b1 = b_lo(c + 1);

@@ -1,16 +1,22 @@
 // tdt_common.cuh -- definitions shared by the TDT loss kernels (sm_103a).
 //
-// Numeric representation of the lattice.  alpha, beta, the log-likelihood
-// and the per-node arc log-weights are 64-bit fixed point with 32 fraction
-// bits ("fx": value * 2^32, rounded).  Additions of fx values are exact and
-// associative, so the long alpha/beta chains ("float64 accumulation for
-// precision on long label sequences", "tdt-loss: add TDT loss kernel",
-// kernels-community PR #882, "What's in it") carry no rounding at all; the
-// only rounding per node is one fp32 exp per incoming arc of a value <= 0 and
-// one fp32 log1p of a value in [0, 1).  GB300 runs float64 at a small
-// fraction of its fp32 rate, which is why the arithmetic per arc is integer
-// + fp32 rather than float64.  |value| < 2^30 holds because log-probs are
-// clamped at -4096, |sigma| <= 1024 and T + U + 1 <= 65536.
+// Numeric representation of the lattice.  The per-node arc log-weights are
+// 64-bit fixed point with 32 fraction bits ("fx": value * 2^32, rounded).
+// alpha, beta and the log-likelihood are pairs (m, s) with value
+// m / 2^32 + ln(s): m an exact fx number, s in [1, 2) in fp32 (s = 0 means
+// -inf).  Adding fx values is exact and associative, so the long alpha/beta
+// chains ("float64 accumulation for precision on long label sequences",
+// "tdt-loss: add TDT loss kernel", kernels-community PR #882, "What's in it")
+// carry no rounding in m; per node, the log-sum-exp over its arcs is
+//   M* = max_j (m_j + w_j)                       exact integer max
+//   S  = sum_j s_j * 2^((m_j + w_j - M*) log2 e)  fp32, S in [1, 4D)
+//   (m, s) = (M* + e ln2, S / 2^e)                e = exponent bits of S
+// so the only rounding per node is one fp32 exp and one multiply-add per
+// arc, and no logarithm, 64-bit conversion or division is needed.  GB300
+// runs float64 (and 64-bit int<->float conversions) at a small fraction of
+// its fp32 rate, which is why the arithmetic is integer + fp32 rather than
+// float64.  |m| < 2^62 holds because log-probs are clamped at -4096,
+// |sigma| <= 1024 and T + U + 1 <= 65536.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -53,21 +59,29 @@ struct Problem {
   long long n_diag;               // T + U1 - 1 anti-diagonals per utterance
 };
 
+// A lattice value m / 2^32 + ln(s) (s = 0, m = 0: -inf), 16 bytes so that
+// one aligned load moves both parts.
+struct __align__(16) LV {
+  fx_t m;
+  float s;
+  float pad;
+};
+
 // Scratch layout (device pointers carved from one workspace block).
 struct Workspace {
-  // anti-diagonal-major tables, index ((b * n_diag + t + u) * U1 + u)
-  fx_t *wb;      // lpB - sigma
-  fx_t *wl;      // lpL - sigma (label y_{u+1}); unused at u = U_b
-  fx_t *lpd;     // [D][B * n_diag * U1] duration log-probs
-  fx_t *alpha;   // [B * n_diag * U1]
-  fx_t *beta;    // [B * n_diag * U1]
+  // anti-diagonal-major, node index g = (b * n_diag + t + u) * U1 + u
+  fx_t *arcw;    // [g][2D] arc log-weights of node g: [i] blank arc with
+                 //   duration i: lpB - sigma + lpD_i; [D + i] label arc with
+                 //   duration i: lpL - sigma + lpD_i (unused at u = U_b)
+  LV *alpha;     // [g]
+  LV *beta;      // [g]
   // node-major per-row data, index n = (b * T + t) * U1 + u
   float *lse_tok;  // log-sum-exp of the token logits
   float *lse_dur;  // log-sum-exp of the duration logits
   float *frac;     // [(2 + D)][nodes]: share of beta(t,u) through blank arcs,
                    //   label arcs, and through each duration
   // per utterance
-  fx_t *loglik;    // [B] log-likelihood from alpha
+  LV *loglik;      // [B] log-likelihood from alpha (s = 0: no path)
   double *scale;   // [B] c_b, factor of dL_b/dz in the reduced loss
   int *usable;     // [B] 1 = lengths and labels usable
 };
@@ -129,6 +143,42 @@ __device__ __forceinline__ fx_t fx_log_ge1(float s) {
 
 __device__ __forceinline__ float fx_to_float(fx_t v) { return __ll2float_rn(v) * (1.0f / 4294967296.0f); }
 
+// An fx difference d <= 0 in log2 units, from two 32-bit conversions (the
+// 64-bit one runs at the float64 rate); below -100 (natural) it is -inf.
+__device__ __forceinline__ float fx_diff_log2(fx_t d) {
+  const int hi = (int)(d >> 32);  // floor(d / 2^32)
+  if (hi < -100) return -INFINITY;
+  const unsigned lo = (unsigned)((unsigned long long)d & 0xffffffffull);
+  return fmaf(__uint2float_rn(lo), kFxToLog2, __int2float_rn(hi) * kLog2e);
+}
+
+// The same with one 32-bit conversion: d rounded to 2^-24 (natural units),
+// which fits 32 bits for d >= -128; below -100 it is -inf.
+__device__ __forceinline__ float fx_diff_log2_fast(fx_t d) {
+  const int hi = (int)(d >> 32);
+  const int v = (int)((d + 128) >> 8);
+  return hi < -100 ? -INFINITY : __int2float_rn(v) * (kLog2e / 16777216.0f);
+}
+
+// Far below any lattice value (|m| < 2^50 for real values) yet safe to add
+// arc weights to: the m of -inf and of missing arcs in the grouped kernel.
+constexpr fx_t kFxVeryNeg = -(1LL << 61);
+
+// (m, s) from an unnormalised sum S >= 1 around the reference M*: pull the
+// exponent bits of S into m (e * ln2, exact in fx), keep the mantissa.
+__device__ __forceinline__ void lv_normalize(float S, fx_t Mstar, fx_t *m, float *s) {
+  const int bits = __float_as_int(S);
+  const int e = (bits >> 23) - 127;
+  *s = __int_as_float((bits & 0x007fffff) | 0x3f800000);
+  *m = Mstar + (fx_t)e * kFxLn2;
+}
+
+__device__ __forceinline__ float fast_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -142,7 +192,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // ---- host side shared by the entry points (tdt_api.cu) ----------------------
 struct Layout {  // byte offsets of the scratch regions inside one block
-  size_t wb, wl, lpd, alpha, beta, lse_tok, lse_dur, frac, loglik, scale, usable, total;
+  size_t arcw, alpha, beta, lse_tok, lse_dur, frac, loglik, scale, usable, total;
 };
 bool make_layout(const int64_t sizes[4], int n_dur, Layout *L);
 Workspace carve(const Layout &L, void *base);

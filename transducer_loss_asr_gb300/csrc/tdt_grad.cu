@@ -55,15 +55,17 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, long long n_beg
   const long long b = bt / p.T;
   E *out = grad + n * p.VD;
   const long long Tb = p.logit_lens[b], Ub = p.label_lens[b];
-  bool live = ws.usable[b] && t < Tb && u <= Ub && ws.loglik[b] != kFxNegInf;
+  bool live = ws.usable[b] && t < Tb && u <= Ub;
   float a = 0.0f;
   if (live) {
+    // N = exp(alpha + beta - logL) = 2^((m_a + m_b - m_L) log2 e) * s_a * s_b / s_L
     const long long q = diag_index(p, b, t, u);
-    const fx_t al = ws.alpha[q], be = ws.beta[q];
-    if (al == kFxNegInf || be == kFxNegInf) {
+    const LV al = ws.alpha[q], be = ws.beta[q], ll = ws.loglik[b];
+    if (al.s == 0.0f || be.s == 0.0f || ll.s == 0.0f) {
       live = false;
     } else {
-      const float occ = fast_exp2(__ll2float_rn(al + be - ws.loglik[b]) * kFxToLog2);
+      const fx_t dm = al.m + be.m - ll.m;
+      const float occ = fast_exp2(__ll2float_rn(dm) * kFxToLog2) * (al.s * be.s / ll.s);
       a = (float)ws.scale[b] * occ;
     }
   }
@@ -96,30 +98,41 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, long long n_beg
       const long long k = tail0 + lane;
       out[k] = Elem<DT>::from_float(g_at(Elem<DT>::load(row + k), k));
     }
-    const char *vin = reinterpret_cast<const char *>(row + head);
-    char *vout = reinterpret_cast<char *>(out + head);
+    const uint4 *vin = reinterpret_cast<const uint4 *>(row + head);
+    uint4 *vout = reinterpret_cast<uint4 *>(out + head);
+    const int nv = (int)nvec;
     // vectors holding the two special entries (or -1)
-    const long long jb = (p.blank >= head && p.blank < tail0) ? (p.blank - head) / N : -1;
-    const long long jy = (y >= head && y < tail0) ? (y - head) / N : -1;
-    for (long long j0 = 0; j0 < nvec; j0 += 32 * kGradUnroll) {
-      uint4 v[kGradUnroll];
+    const int jb = (p.blank >= head && p.blank < tail0) ? (int)((p.blank - head) / N) : -1;
+    const int jy = (y >= head && y < tail0) ? (int)((y - head) / N) : -1;
+    const int eb = (int)((p.blank - head) % N), ey = (int)((y - head) % N);
+    // Two batches of kGradUnroll vectors per lane: the next batch is loaded
+    // before the current one is computed and stored.
+    uint4 cur[kGradUnroll], nxt[kGradUnroll];
+#pragma unroll
+    for (int k = 0; k < kGradUnroll; ++k) {
+      const int j = k * 32 + lane;
+      if (j < nv) cur[k] = __ldg(vin + j);
+    }
+    for (int j0 = 0; j0 < nv; j0 += 32 * kGradUnroll) {
+      const int jn = j0 + 32 * kGradUnroll;
 #pragma unroll
       for (int k = 0; k < kGradUnroll; ++k) {
-        const long long j = j0 + k * 32 + lane;
-        if (j < nvec) v[k] = ld_vec(vin + j * 16);
+        const int j = jn + k * 32 + lane;
+        if (j < nv) nxt[k] = __ldg(vin + j);
       }
 #pragma unroll
       for (int k = 0; k < kGradUnroll; ++k) {
-        const long long j = j0 + k * 32 + lane;
-        if (j < nvec) {
+        const int j = j0 + k * 32 + lane;
+        if (j < nv) {
           float x[N];
-          unpack<DT>(v[k], x);
+          unpack<DT>(cur[k], x);
 #pragma unroll
           for (int e = 0; e < N; ++e) x[e] = a * fast_exp2(fmaf(x[e], kLog2e, -lse2));
-          if (j == jb) x[(p.blank - head) % N] -= ab;
-          if (j == jy) x[(y - head) % N] -= al;
-          *reinterpret_cast<uint4 *>(vout + j * 16) = pack<DT>(x);
+          if (j == jb) x[eb] -= ab;
+          if (j == jy) x[ey] -= al;
+          vout[j] = pack<DT>(x);
         }
+        cur[k] = nxt[k];
       }
     }
   } else {

@@ -12,9 +12,10 @@
 // between them.
 //
 // Outputs per usable node (t < T_b, u <= U_b):
-//   lse_tok[n], lse_dur[n]         float, for the gradient pass
-//   wb = lpB - sigma, wl = lpL - sigma, lpd[i]   fx, anti-diagonal layout,
-//                                   for the alpha/beta passes
+//   lse_tok[n], lse_dur[n]   float, for the gradient pass
+//   arcw[g][0..2D)           fx arc log-weights lpB - sigma + lpD_i and
+//                            lpL - sigma + lpD_i, anti-diagonal layout, one
+//                            contiguous record per node for the lattice passes
 #include "tdt_rowio.cuh"
 
 namespace tdt {
@@ -61,14 +62,28 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
     m = Elem<DT>::load(row + tail0 + (lane - head));
     s = 1.0f;
   }
-  const char *vbase = reinterpret_cast<const char *>(row + head);
-  for (long long j0 = 0; j0 < nvec; j0 += 32 * kTablesUnroll) {
+  // Two batches of kTablesUnroll 16-byte vectors per lane: the next batch is
+  // loaded before the math of the current one, so loads stay in flight.
+  const uint4 *vbase = reinterpret_cast<const uint4 *>(row + head);
+  const int nv = (int)nvec;
+  uint4 cur[kTablesUnroll], nxt[kTablesUnroll];
+#pragma unroll
+  for (int k = 0; k < kTablesUnroll; ++k) {
+    const int j = k * 32 + lane;
+    if (j < nv) cur[k] = __ldg(vbase + j);
+  }
+  for (int j0 = 0; j0 < nv; j0 += 32 * kTablesUnroll) {
+    const int jn = j0 + 32 * kTablesUnroll;
+#pragma unroll
+    for (int k = 0; k < kTablesUnroll; ++k) {
+      const int j = jn + k * 32 + lane;
+      if (j < nv) nxt[k] = __ldg(vbase + j);
+    }
     float x[kTablesUnroll * N];
 #pragma unroll
     for (int k = 0; k < kTablesUnroll; ++k) {
-      const long long j = j0 + k * 32 + lane;
-      if (j < nvec) {
-        unpack<DT>(ld_vec(vbase + j * 16), x + k * N);
+      if (j0 + k * 32 + lane < nv) {
+        unpack<DT>(cur[k], x + k * N);
       } else {
 #pragma unroll
         for (int e = 0; e < N; ++e) x[k * N + e] = -INFINITY;
@@ -86,6 +101,8 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
 #pragma unroll
       for (int e = 0; e < kTablesUnroll * N; ++e) s += fast_exp2((x[e] - m) * kLog2e);
     }
+#pragma unroll
+    for (int k = 0; k < kTablesUnroll; ++k) cur[k] = nxt[k];
   }
   const float M = warp_max(m);
   const float S = warp_sum(m == -INFINITY ? 0.0f : s * fast_exp2((m - M) * kLog2e));
@@ -97,21 +114,27 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
   const float Sd = warp_sum(lane < p.D ? fast_exp2((zd - Md) * kLog2e) : 0.0f);
   const fx_t lsed_fx = fx_from_float(Md) + fx_log_ge1(Sd);
 
-  const long long q = diag_index(p, b, t, u);
-  const long long ndiag_total = p.B * p.n_diag * p.U1;
-  if (lane < p.D) ws.lpd[(long long)lane * ndiag_total + q] = clamp_lp(fx_from_float(zd) - lsed_fx);
+  // arc log-weights of this node: [i] blank arc with duration i, [D + i]
+  // label arc with duration i (lane i writes both)
+  fx_t wbs = 0, wls = 0;
   if (lane == 0) {
     const float zb = Elem<DT>::load(row + p.blank);
-    ws.wb[q] = clamp_lp(fx_from_float(zb) - lse_fx) - p.sigma_fx;
-    fx_t wl = kFxNegInf;
+    wbs = clamp_lp(fx_from_float(zb) - lse_fx) - p.sigma_fx;
     if (u < Ub) {
       const long long y = p.labels[b * (p.U1 - 1) + u];
       if (y >= 0 && y < p.V && y != p.blank)
-        wl = clamp_lp(fx_from_float(Elem<DT>::load(row + y)) - lse_fx) - p.sigma_fx;
+        wls = clamp_lp(fx_from_float(Elem<DT>::load(row + y)) - lse_fx) - p.sigma_fx;
     }
-    ws.wl[q] = wl;
     ws.lse_tok[n] = M + logf(S);
     ws.lse_dur[n] = Md + logf(Sd);
+  }
+  wbs = __shfl_sync(0xffffffffu, wbs, 0);
+  wls = __shfl_sync(0xffffffffu, wls, 0);
+  if (lane < p.D) {
+    const fx_t ld = clamp_lp(fx_from_float(zd) - lsed_fx);
+    fx_t *rec = ws.arcw + diag_index(p, b, t, u) * (2 * p.D);
+    rec[lane] = wbs + ld;
+    rec[p.D + lane] = wls + ld;
   }
 }
 
