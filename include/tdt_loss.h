@@ -29,7 +29,7 @@
  *               W > V+D).  Token logits are [..., 0:V) with `blank` inside,
  *               duration logits [..., V:V+D), D = n_dur.
  *   sizes       host, {B, T, U+1, V+D}; B >= 0, T >= 1, U+1 >= 1,
- *               V+D > n_dur, T + U + 1 <= 65536.
+ *               V+D > n_dur, T + U + 1 <= 65536, B * T * (U+1) < 2^31.
  *   labels      device int64 [B, U] contiguous (U = sizes[2]-1); entries at
  *               u >= label_lens[b] are ignored (-100 padding).  May be NULL
  *               when U = 0.

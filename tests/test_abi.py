@@ -99,6 +99,7 @@ def _call(lib, **over):
     (dict(sizes=[-1, 5, 3, 10]), -2),
     (dict(sizes=[2, 5, 3, 3]), -2),             # V + D must exceed n_dur
     (dict(sizes=[1, 60000, 6000, 10]), -2),     # T + U + 1 > 65536
+    (dict(sizes=[1 << 20, 64, 32, 10]), -2),    # B * T * (U+1) >= 2^31
     (dict(strides=[150, 30, 10, 2]), -3),
     (dict(strides=[150, -30, 10, 1]), -3),
     (dict(durations=[]), -5),

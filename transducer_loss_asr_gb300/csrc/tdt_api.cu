@@ -23,6 +23,7 @@ namespace tdt {
 namespace {
 
 size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
+int row_coeff_stride(int n_dur) { return (kRcD + n_dur + 3) & ~3; }
 
 }  // namespace
 
@@ -44,6 +45,7 @@ bool make_layout(const int64_t sizes[4], int n_dur, Layout *L) {
   L->beta = take(ndiag * sizeof(LV));
   L->lse_tok = take(nodes * 4);
   L->lse_dur = take(nodes * 4);
+  L->rowc = take(nodes * 4 * (size_t)row_coeff_stride(n_dur));
   L->frac = take(nodes * 4 * (size_t)(2 + n_dur));
   L->loglik = take((size_t)B * sizeof(LV));
   L->scale = take((size_t)B * 8);
@@ -60,6 +62,7 @@ Workspace carve(const Layout &L, void *base) {
   w.beta = reinterpret_cast<LV *>(c + L.beta);
   w.lse_tok = reinterpret_cast<float *>(c + L.lse_tok);
   w.lse_dur = reinterpret_cast<float *>(c + L.lse_dur);
+  w.rowc = reinterpret_cast<float *>(c + L.rowc);
   w.frac = reinterpret_cast<float *>(c + L.frac);
   w.loglik = reinterpret_cast<LV *>(c + L.loglik);
   w.scale = reinterpret_cast<double *>(c + L.scale);
@@ -83,6 +86,7 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
   const long long B = sizes[0], T = sizes[1], U1 = sizes[2], VD = sizes[3];
   if (B < 0 || T < 1 || U1 < 1 || VD <= n_dur) return TDT_ERR_BAD_SIZES;
   if (T + U1 > 65536) return TDT_ERR_BAD_SIZES;
+  if (B * T * U1 >= (1LL << 31)) return TDT_ERR_BAD_SIZES;
   if (B > 0 && (!logits || !logit_lens || !label_lens)) return TDT_ERR_NULL_POINTER;
   if (B > 0 && U1 > 1 && !labels) return TDT_ERR_NULL_POINTER;
   if (strides[3] != 1 || strides[0] < 0 || strides[1] < 0 || strides[2] < 0)
@@ -118,6 +122,7 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
   p->reduction = reduction;
   p->sigma_fx = (fx_t)llround(sigma * kFxOne);
   p->n_diag = T + U1 - 1;
+  p->rc_stride = row_coeff_stride(n_dur);
   return TDT_OK;
 }
 
@@ -234,6 +239,8 @@ int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void 
     TDT_TRY(cudaStreamWaitEvent(side, res->tables_done[c], 0));
     TDT_TRY(timed(TDT_KERNEL_LATTICE, side,
                   [&] { return launch_lattice(p, ws, b0, b1, with_grad, side); }));
+    if (with_grad)
+      TDT_TRY(launch_row_coeffs(p, ws, b0 * rows_per_utt, b1 * rows_per_utt, side));
     TDT_TRY(cudaEventRecord(res->lattice_done[c], side));
   }
   // the reduction needs every chunk's log-likelihood; it joins all side streams

@@ -57,7 +57,25 @@ struct Problem {
   int reduction;
   fx_t sigma_fx;
   long long n_diag;               // T + U1 - 1 anti-diagonals per utterance
+  int rc_stride;                  // floats per row-coefficient record
 };
+
+// Row-coefficient record (floats) the gradient pass reads for node n:
+enum RowCoeff {
+  kRcA = 0,      // c_b * N(t,u)   (N = occupancy exp(alpha + beta - logL))
+  kRcLse2 = 1,   // log2 e * log-sum-exp of the token logits
+  kRcLsed2 = 2,  // log2 e * log-sum-exp of the duration logits
+  kRcAB = 3,     // c_b N fB: taken off the blank entry
+  kRcAL = 4,     // c_b N fL: taken off the label entry
+  kRcY = 5,      // label y_{u+1} as int bits (-1: none)
+  kRcLive = 6,   // 1: row inside a usable lattice with N > 0, 0: write zeros
+  kRcD = 8,      // [kRcD + i] = c_b N fD_i
+};
+// Shared memory a K1/K4 block reserves without using it: with it, no K1/K4
+// block fits beside a lattice block (which requests kLatticeSmemFloor), so
+// the latency-bound lattice passes get SMs of their own.
+constexpr int kStreamSmemReserve = 32 * 1024;
+constexpr int kLatticeSmemFloor = 200 * 1024;
 
 // A lattice value m / 2^32 + ln(s) (s = 0, m = 0: -inf), 16 bytes so that
 // one aligned load moves both parts.
@@ -78,6 +96,7 @@ struct Workspace {
   // node-major per-row data, index n = (b * T + t) * U1 + u
   float *lse_tok;  // log-sum-exp of the token logits
   float *lse_dur;  // log-sum-exp of the duration logits
+  float *rowc;     // [nodes][rc_stride] row-coefficient records (RowCoeff)
   float *frac;     // [(2 + D)][nodes]: share of beta(t,u) through blank arcs,
                    //   label arcs, and through each duration
   // per utterance
@@ -89,6 +108,18 @@ struct Workspace {
 __host__ __device__ inline long long diag_index(const Problem &p, long long b, long long t,
                                                 long long u) {
   return (b * p.n_diag + t + u) * p.U1 + u;
+}
+
+// (b, t, u) of node n = (b * T + t) * U1 + u with 32-bit divisions (64-bit
+// ones are long software sequences); B * T * U1 < 2^31 is checked on the host.
+__device__ __forceinline__ void decode_node(const Problem &p, long long n, long long *b,
+                                            long long *t, long long *u) {
+  const unsigned nn = (unsigned)n, U1 = (unsigned)p.U1, T = (unsigned)p.T;
+  const unsigned bt = nn / U1;
+  *u = nn - bt * U1;
+  const unsigned bb = bt / T;
+  *t = bt - bb * T;
+  *b = bb;
 }
 
 // ---- element access -------------------------------------------------------
@@ -192,7 +223,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // ---- host side shared by the entry points (tdt_api.cu) ----------------------
 struct Layout {  // byte offsets of the scratch regions inside one block
-  size_t arcw, alpha, beta, lse_tok, lse_dur, frac, loglik, scale, usable, total;
+  size_t arcw, alpha, beta, lse_tok, lse_dur, rowc, frac, loglik, scale, usable, total;
 };
 bool make_layout(const int64_t sizes[4], int n_dur, Layout *L);
 Workspace carve(const Layout &L, void *base);
@@ -211,5 +242,7 @@ cudaError_t launch_reduce(const Problem &p, const Workspace &ws, float *loss_out
                           cudaStream_t stream);
 cudaError_t launch_grad(const Problem &p, int dtype, const Workspace &ws, void *grad_out,
                         long long n_begin, long long n_end, cudaStream_t stream);
+cudaError_t launch_row_coeffs(const Problem &p, const Workspace &ws, long long n_begin,
+                              long long n_end, cudaStream_t stream);
 
 }  // namespace tdt

@@ -10,9 +10,13 @@
 // The softmaxes are recomputed from the row and the saved log-sum-exps, so
 // the row is read once more and every gradient element written once, in the
 // input dtype (round to nearest).  Rows outside a lattice are written as 0.
-// One warp per row; 16-byte loads and stores when the input row and the
-// output row have the same offset from a 16-byte boundary (the contiguous
-// case), coalesced scalar accesses otherwise.
+// A group of TPR threads takes one row (the same grouping as the node-table
+// pass): each thread issues kBatch independent 16-byte loads, then computes
+// and stores them as 16-byte vectors, when the input row and the output row
+// sit at the same offset from a 16-byte boundary (the contiguous case);
+// coalesced scalar accesses otherwise.  The first batch of a row is loaded
+// before the row's coefficient record (written by row_coeff_kernel after the
+// lattice pass), so their latencies overlap.
 #include "tdt_rowio.cuh"
 
 namespace tdt {
@@ -20,40 +24,138 @@ namespace tdt {
 namespace {
 
 constexpr int kGradThreads = 256;
-constexpr int kGradUnroll = 4;
-constexpr int kScalarUnroll = 8;
+constexpr int kBatch = 8;
+constexpr int kVecPerThread = 8;  // one batch per thread for long rows
 
-template <int DT>
-__device__ __forceinline__ void zero_row(typename Elem<DT>::T *out, long long VD, int lane) {
+template <int DT, int TPR>
+__device__ __forceinline__ void zero_row(typename Elem<DT>::T *out, long long VD, int lt) {
   typedef typename Elem<DT>::T E;
   constexpr int N = Vec<DT>::N;
   int head = head_elems<DT>(out);
   if (head > VD) head = (int)VD;
-  const long long nvec = (VD - head) / N;
-  const long long tail0 = head + nvec * N;
+  const int nvec = (int)((VD - head) / N);
+  const long long tail0 = head + (long long)nvec * N;
   const E zero = Elem<DT>::from_float(0.0f);
-  if (lane < head) out[lane] = zero;
-  if (lane < VD - tail0) out[tail0 + lane] = zero;
+  if (lt < head) out[lt] = zero;
+  if (lt < VD - tail0) out[tail0 + lt] = zero;
   uint4 *v = reinterpret_cast<uint4 *>(out + head);
-  for (long long j = lane; j < nvec; j += 32) v[j] = make_uint4(0u, 0u, 0u, 0u);
+  for (int j = lt; j < nvec; j += TPR) v[j] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-template <int DT>
+template <int DT, int TPR>
 __global__ void __launch_bounds__(kGradThreads)
 grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, long long n_begin,
             long long n_end) {
   typedef typename Elem<DT>::T E;
   constexpr int N = Vec<DT>::N;
+  constexpr int RPB = kGradThreads / TPR;
   const E *logits = static_cast<const E *>(p.logits);
-  const int lane = threadIdx.x & 31;
-  const long long n = n_begin + (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int lt = threadIdx.x % TPR;
+  const long long n = n_begin + (long long)blockIdx.x * RPB + threadIdx.x / TPR;
+  if (n >= n_end) return;
+  long long b, t, u;
+  decode_node(p, n, &b, &t, &u);
+  E *out = grad + n * p.VD;
+  const long long Tb = p.logit_lens[b], Ub = p.label_lens[b];
+  const E *row = logits + b * p.s0 + t * p.s1 + u * p.s2;
+  const bool in_lattice = t < Tb && u <= Ub;
+  // Row geometry, and the first batch of 16-byte loads issued before the
+  // per-row coefficients are fetched, so the two latencies overlap.
+  const uintptr_t ai = reinterpret_cast<uintptr_t>(row), ao = reinterpret_cast<uintptr_t>(out);
+  const bool vec = ((ai ^ ao) & 15) == 0;
+  int head = head_elems<DT>(row);
+  if (head > p.V) head = (int)p.V;
+  const int nvec = (int)((p.V - head) / N);
+  const uint4 *vin = reinterpret_cast<const uint4 *>(row + head);
+  uint4 v[kBatch];
+  if (in_lattice && vec) {
+#pragma unroll
+    for (int i = 0; i < kBatch; ++i) {
+      const int j = i * TPR + lt;
+      if (j < nvec) v[i] = __ldg(vin + j);
+    }
+  }
+  const float *rc = ws.rowc + n * p.rc_stride;
+  const float4 r0 = *reinterpret_cast<const float4 *>(rc);
+  const float4 r1 = *reinterpret_cast<const float4 *>(rc + 4);
+  if (!in_lattice || r1.z == 0.0f) {
+    zero_row<DT, TPR>(out, p.VD, lt);
+    return;
+  }
+  const float a = r0.x, lse2 = r0.y, lsed2 = r0.z, ab = r0.w, al = r1.x;
+  const int y = __float_as_int(r1.y);
+  auto g_at = [&](float x, long long k) {
+    float g = a * fast_exp2(fmaf(x, kLog2e, -lse2));
+    if (k == p.blank) g -= ab;
+    if (k == y) g -= al;
+    return g;
+  };
+
+  if (vec) {
+    const long long tail0 = head + (long long)nvec * N;
+    const int ntail = (int)(p.V - tail0);
+    if (lt < head) out[lt] = Elem<DT>::from_float(g_at(Elem<DT>::load(row + lt), lt));
+    if (lt < ntail) {
+      const long long k = tail0 + lt;
+      out[k] = Elem<DT>::from_float(g_at(Elem<DT>::load(row + k), k));
+    }
+    uint4 *vout = reinterpret_cast<uint4 *>(out + head);
+    // vectors holding the two special entries (or -1)
+    const int jb = (p.blank >= head && p.blank < tail0) ? (int)((p.blank - head) / N) : -1;
+    const int jy = (y >= head && y < tail0) ? (int)((y - head) / N) : -1;
+    const int eb = (int)((p.blank - head) % N), ey = (int)((y - head) % N);
+    for (int j0 = 0; j0 < nvec; j0 += TPR * kBatch) {
+      if (j0 > 0) {
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          const int j = j0 + i * TPR + lt;
+          if (j < nvec) v[i] = __ldg(vin + j);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const int j = j0 + i * TPR + lt;
+        if (j < nvec) {
+          float x[N];
+          unpack<DT>(v[i], x);
+#pragma unroll
+          for (int e = 0; e < N; ++e) x[e] = a * fast_exp2(fmaf(x[e], kLog2e, -lse2));
+          if (j == jb) x[eb] -= ab;
+          if (j == jy) x[ey] -= al;
+          vout[j] = pack<DT>(x);
+        }
+      }
+    }
+  } else {
+    for (long long k0 = 0; k0 < p.V; k0 += TPR * kBatch) {
+      float x[kBatch];
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const long long k = k0 + i * TPR + lt;
+        x[i] = (k < p.V) ? Elem<DT>::load(row + k) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < kBatch; ++i) {
+        const long long k = k0 + i * TPR + lt;
+        if (k < p.V) out[k] = Elem<DT>::from_float(g_at(x[i], k));
+      }
+    }
+  }
+  for (int i = lt; i < p.D; i += TPR) {
+    const float zd = Elem<DT>::load(row + p.V + i);
+    out[p.V + i] = Elem<DT>::from_float(a * fast_exp2(fmaf(zd, kLog2e, -lsed2)) - rc[kRcD + i]);
+  }
+}
+
+// Row-coefficient records for rows [n_begin, n_end): everything the gradient
+// pass needs about a node besides its logits row, in one record per row.
+__global__ void row_coeff_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) {
+  const long long n = n_begin + (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= n_end) return;
   const long long nodes = p.B * p.T * p.U1;
-  const long long u = n % p.U1;
-  const long long bt = n / p.U1;
-  const long long t = bt % p.T;
-  const long long b = bt / p.T;
-  E *out = grad + n * p.VD;
+  long long b, t, u;
+  decode_node(p, n, &b, &t, &u);
+  float *rc = ws.rowc + n * p.rc_stride;
   const long long Tb = p.logit_lens[b], Ub = p.label_lens[b];
   bool live = ws.usable[b] && t < Tb && u <= Ub;
   float a = 0.0f;
@@ -70,117 +172,69 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, long long n_beg
     }
   }
   if (!live) {
-    zero_row<DT>(out, p.VD, lane);
+    rc[kRcLive] = 0.0f;
     return;
   }
-  const E *row = logits + b * p.s0 + t * p.s1 + u * p.s2;
-  const float lse2 = ws.lse_tok[n] * kLog2e;
-  const float lsed2 = ws.lse_dur[n] * kLog2e;
-  const float ab = a * ws.frac[n];           // a * fB, taken off the blank entry
-  const float al = a * ws.frac[nodes + n];   // a * fL, taken off the label entry
-  const long long y = (u < Ub) ? p.labels[b * (p.U1 - 1) + u] : -1;
-  auto g_at = [&](float x, long long k) {
-    float g = a * fast_exp2(fmaf(x, kLog2e, -lse2));
-    if (k == p.blank) g -= ab;
-    if (k == y) g -= al;
-    return g;
-  };
+  const int y = (u < Ub) ? (int)p.labels[b * (p.U1 - 1) + u] : -1;
+  float4 r0, r1;
+  r0.x = a;
+  r0.y = ws.lse_tok[n] * kLog2e;
+  r0.z = ws.lse_dur[n] * kLog2e;
+  r0.w = a * ws.frac[n];
+  r1.x = a * ws.frac[nodes + n];
+  r1.y = __int_as_float(y);
+  r1.z = 1.0f;
+  r1.w = 0.0f;
+  *reinterpret_cast<float4 *>(rc) = r0;
+  *reinterpret_cast<float4 *>(rc + 4) = r1;
+  for (int i = 0; i < p.D; ++i) rc[kRcD + i] = a * ws.frac[(long long)(2 + i) * nodes + n];
+}
 
-  const uintptr_t ai = reinterpret_cast<uintptr_t>(row), ao = reinterpret_cast<uintptr_t>(out);
-  if (((ai ^ ao) & 15) == 0) {
-    int head = head_elems<DT>(row);
-    if (head > p.V) head = (int)p.V;
-    const long long nvec = (p.V - head) / N;
-    const long long tail0 = head + nvec * N;
-    const int ntail = (int)(p.V - tail0);
-    if (lane < head) out[lane] = Elem<DT>::from_float(g_at(Elem<DT>::load(row + lane), lane));
-    if (lane < ntail) {
-      const long long k = tail0 + lane;
-      out[k] = Elem<DT>::from_float(g_at(Elem<DT>::load(row + k), k));
-    }
-    const uint4 *vin = reinterpret_cast<const uint4 *>(row + head);
-    uint4 *vout = reinterpret_cast<uint4 *>(out + head);
-    const int nv = (int)nvec;
-    // vectors holding the two special entries (or -1)
-    const int jb = (p.blank >= head && p.blank < tail0) ? (int)((p.blank - head) / N) : -1;
-    const int jy = (y >= head && y < tail0) ? (int)((y - head) / N) : -1;
-    const int eb = (int)((p.blank - head) % N), ey = (int)((y - head) % N);
-    // Two batches of kGradUnroll vectors per lane: the next batch is loaded
-    // before the current one is computed and stored.
-    uint4 cur[kGradUnroll], nxt[kGradUnroll];
-#pragma unroll
-    for (int k = 0; k < kGradUnroll; ++k) {
-      const int j = k * 32 + lane;
-      if (j < nv) cur[k] = __ldg(vin + j);
-    }
-    for (int j0 = 0; j0 < nv; j0 += 32 * kGradUnroll) {
-      const int jn = j0 + 32 * kGradUnroll;
-#pragma unroll
-      for (int k = 0; k < kGradUnroll; ++k) {
-        const int j = jn + k * 32 + lane;
-        if (j < nv) nxt[k] = __ldg(vin + j);
-      }
-#pragma unroll
-      for (int k = 0; k < kGradUnroll; ++k) {
-        const int j = j0 + k * 32 + lane;
-        if (j < nv) {
-          float x[N];
-          unpack<DT>(cur[k], x);
-#pragma unroll
-          for (int e = 0; e < N; ++e) x[e] = a * fast_exp2(fmaf(x[e], kLog2e, -lse2));
-          if (j == jb) x[eb] -= ab;
-          if (j == jy) x[ey] -= al;
-          vout[j] = pack<DT>(x);
-        }
-        cur[k] = nxt[k];
-      }
-    }
-  } else {
-    for (long long k0 = 0; k0 < p.V; k0 += 32 * kScalarUnroll) {
-      float x[kScalarUnroll];
-#pragma unroll
-      for (int j = 0; j < kScalarUnroll; ++j) {
-        const long long k = k0 + j * 32 + lane;
-        x[j] = (k < p.V) ? Elem<DT>::load(row + k) : 0.0f;
-      }
-#pragma unroll
-      for (int j = 0; j < kScalarUnroll; ++j) {
-        const long long k = k0 + j * 32 + lane;
-        if (k < p.V) out[k] = Elem<DT>::from_float(g_at(x[j], k));
-      }
-    }
-  }
-  if (lane < p.D) {
-    const float zd = Elem<DT>::load(row + p.V + lane);
-    const float g = fast_exp2(fmaf(zd, kLog2e, -lsed2)) - ws.frac[(long long)(2 + lane) * nodes + n];
-    out[p.V + lane] = Elem<DT>::from_float(a * g);
+template <int DT, int TPR>
+cudaError_t launch_tpr(const Problem &p, const Workspace &ws, typename Elem<DT>::T *grad,
+                       long long n_begin, long long n_end, cudaStream_t stream) {
+  constexpr int RPB = kGradThreads / TPR;
+  const long long rows = n_end - n_begin;
+  const long long blocks = (rows + RPB - 1) / RPB;
+  grad_kernel<DT, TPR><<<(unsigned)blocks, kGradThreads, kStreamSmemReserve, stream>>>(
+      p, ws, grad, n_begin, n_end);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_dt(const Problem &p, const Workspace &ws, void *grad_out, long long n_begin,
+                      long long n_end, cudaStream_t stream) {
+  typedef typename Elem<DT>::T E;
+  E *g = static_cast<E *>(grad_out);
+  const int tpr = row_group_threads(p.V * (long long)sizeof(E), kVecPerThread);
+  switch (tpr) {
+    case 8: return launch_tpr<DT, 8>(p, ws, g, n_begin, n_end, stream);
+    case 16: return launch_tpr<DT, 16>(p, ws, g, n_begin, n_end, stream);
+    case 32: return launch_tpr<DT, 32>(p, ws, g, n_begin, n_end, stream);
+    case 64: return launch_tpr<DT, 64>(p, ws, g, n_begin, n_end, stream);
+    case 128: return launch_tpr<DT, 128>(p, ws, g, n_begin, n_end, stream);
+    default: return launch_tpr<DT, 256>(p, ws, g, n_begin, n_end, stream);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_grad(const Problem &p, int dtype, const Workspace &ws, void *grad_out,
-                        long long n_begin, long long n_end, cudaStream_t stream) {
+cudaError_t launch_row_coeffs(const Problem &p, const Workspace &ws, long long n_begin,
+                              long long n_end, cudaStream_t stream) {
   const long long rows = n_end - n_begin;
   if (rows <= 0) return cudaSuccess;
-  const long long warps_per_block = kGradThreads / 32;
-  const long long blocks = (rows + warps_per_block - 1) / warps_per_block;
-  dim3 grid((unsigned)blocks), block(kGradThreads);
-  switch (dtype) {
-    case kF32:
-      grad_kernel<kF32><<<grid, block, 0, stream>>>(p, ws, static_cast<float *>(grad_out),
-                                                    n_begin, n_end);
-      break;
-    case kF16:
-      grad_kernel<kF16><<<grid, block, 0, stream>>>(p, ws, static_cast<__half *>(grad_out),
-                                                    n_begin, n_end);
-      break;
-    default:
-      grad_kernel<kBF16><<<grid, block, 0, stream>>>(
-          p, ws, static_cast<__nv_bfloat16 *>(grad_out), n_begin, n_end);
-      break;
-  }
+  row_coeff_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(p, ws, n_begin, n_end);
   return cudaGetLastError();
+}
+
+cudaError_t launch_grad(const Problem &p, int dtype, const Workspace &ws, void *grad_out,
+                        long long n_begin, long long n_end, cudaStream_t stream) {
+  if (n_end - n_begin <= 0) return cudaSuccess;
+  switch (dtype) {
+    case kF32: return launch_dt<kF32>(p, ws, grad_out, n_begin, n_end, stream);
+    case kF16: return launch_dt<kF16>(p, ws, grad_out, n_begin, n_end, stream);
+    default: return launch_dt<kBF16>(p, ws, grad_out, n_begin, n_end, stream);
+  }
 }
 
 }  // namespace tdt

@@ -29,8 +29,9 @@ namespace {
 
 constexpr int kLatticeMaxThreads = 1024;
 constexpr int kPrefetch = 6;
-// Lanes per lattice node in the grouped shared-ring variant.
-constexpr int kGroup = 4;
+// Lanes per lattice node in the grouped shared-ring variant: 8 when a
+// node's durations fit one per lane and the block fits, else 4.
+constexpr int kGroupMax = 8;
 
 __device__ __forceinline__ fx_t fmax_fx(fx_t a, fx_t b) { return a > b ? a : b; }
 
@@ -303,39 +304,39 @@ template <int ND> struct Rings {
 // Start the copies of diagonal q's record of node u (if it is a lattice
 // node): lane k of the group copies the 16-byte chunks k, k+G, ...; every
 // lane commits one group per call so the group count per step is fixed.
-template <int ND>
+template <int ND, int G>
 __device__ __forceinline__ void prefetch_group(const fx_t *gdiag0, const Rings<ND> &r, int q,
                                                int u, int k, int Tb, int Ub, int U1) {
   const int t = q - u;
   if (q >= 0 && u <= Ub && t >= 0 && t < Tb) {
     const fx_t *src = gdiag0 + ((long long)q * U1 + u) * (2 * ND);
     fx_t *dst = r.W + ((q & r.mW) * r.U1p + u) * (2 * ND);
-    for (int c = k; c < ND; c += kGroup) cp_async16(dst + 2 * c, src + 2 * c);
+    for (int c = k; c < ND; c += G) cp_async16(dst + 2 * c, src + 2 * c);
   }
   cp_async_commit();
 }
 
-// Grouped variant: lane k of a node's group of kGroup lanes handles
+// Grouped variant: lane k of a node's group of G lanes handles
 // durations k, k+G, ... (both the blank and the label arc of each), so every
 // lane runs the same instructions; the int64 max and the fp32 sum are
 // combined across the group with xor shuffles.
 
-template <int ND>
+template <int ND, int G>
 struct GroupArcs {
-  static constexpr int J = (ND + kGroup - 1) / kGroup;  // durations per lane
+  static constexpr int J = (ND + G - 1) / G;  // durations per lane
 };
 
 // Group-wide log-sum-exp of this lane's 2J candidates; returns the group's
 // M* and S (S = 0 when the group has no finite candidate) and each
 // candidate's unnormalised term.
-template <int J>
+template <int J, int G>
 __device__ __forceinline__ void group_lse(const fx_t *M, const float *S, fx_t *ms_out,
                                           float *tot_out, float *term) {
   fx_t ms = M[0];
 #pragma unroll
   for (int j = 1; j < 2 * J; ++j) ms = fmax_fx(ms, M[j]);
 #pragma unroll
-  for (int o = 1; o < kGroup; o <<= 1) ms = fmax_fx(ms, __shfl_xor_sync(0xffffffffu, ms, o));
+  for (int o = 1; o < G; o <<= 1) ms = fmax_fx(ms, __shfl_xor_sync(0xffffffffu, ms, o));
   float tot = 0.0f;
 #pragma unroll
   for (int j = 0; j < 2 * J; ++j) {
@@ -343,29 +344,33 @@ __device__ __forceinline__ void group_lse(const fx_t *M, const float *S, fx_t *m
     tot += term[j];
   }
 #pragma unroll
-  for (int o = 1; o < kGroup; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+  for (int o = 1; o < G; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
   *ms_out = ms;
   *tot_out = tot;
 }
 
-template <int ND>
+template <int ND, int G>
 __device__ void alpha_grouped(const Problem &p, const Workspace &ws, const Rings<ND> &r,
                               long long b, int Tb, int Ub) {
-  constexpr int J = GroupArcs<ND>::J;
-  const int u = threadIdx.x / kGroup, k = threadIdx.x % kGroup;
+  constexpr int J = GroupArcs<ND, G>::J;
+  const int u = threadIdx.x / G, k = threadIdx.x % G;
+  // node index for ring reads: threads past the last row (u >= U+1, in the
+  // last warp) only join the barriers, and read row U1p - 1 so every read
+  // stays in bounds
+  const int uc = u < r.U1p ? u : r.U1p - 1;
   const int U1 = (int)p.U1;
   const fx_t *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * (2 * ND);
   LV *galpha = ws.alpha + b * p.n_diag * p.U1;
   int di[J], dd[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) {
-    di[j] = k + kGroup * j;
+    di[j] = k + G * j;
     dd[j] = di[j] < ND ? p.dur[di[j]] : -1;
   }
   const int nsteps = Tb + Ub;
-  for (int q = 0; q < kPrefetch; ++q) prefetch_group<ND>(gdiag0, r, q, u, k, Tb, Ub, U1);
+  for (int q = 0; q < kPrefetch; ++q) prefetch_group<ND, G>(gdiag0, r, q, u, k, Tb, Ub, U1);
   for (int s = 0; s < nsteps; ++s) {
-    prefetch_group<ND>(gdiag0, r, s + kPrefetch, u, k, Tb, Ub, U1);
+    prefetch_group<ND, G>(gdiag0, r, s + kPrefetch, u, k, Tb, Ub, U1);
     cp_async_wait<kPrefetch>();
     __syncthreads();
     const int t = s - u;
@@ -377,13 +382,13 @@ __device__ void alpha_grouped(const Problem &p, const Workspace &ws, const Rings
       const int d = dd[j];
       // blank arc (t-d, u) -> (t, u), d > 0
       const bool okb = node && d > 0 && t - d >= 0;
-      const LV ab = r.a(s - d, u);
-      const fx_t wb = r.w(s - d, u)[di[j] < ND ? di[j] : 0];
+      const LV ab = r.a(s - d, uc);
+      const fx_t wb = r.w(s - d, uc)[di[j] < ND ? di[j] : 0];
       M[2 * j] = okb ? ab.m + wb : kFxVeryNeg;
       S[2 * j] = okb ? ab.s : 0.0f;
       // label arc (t-d, u-1) -> (t, u), every d
       const bool okl = node && d >= 0 && u >= 1 && t - d >= 0;
-      const int ul = u >= 1 ? u - 1 : 0;
+      const int ul = uc >= 1 ? uc - 1 : 0;
       const LV al = r.a(s - d - 1, ul);
       const fx_t wl = r.w(s - d - 1, ul)[di[j] < ND ? ND + di[j] : 0];
       M[2 * j + 1] = okl ? al.m + wl : kFxVeryNeg;
@@ -391,7 +396,7 @@ __device__ void alpha_grouped(const Problem &p, const Workspace &ws, const Rings
     }
     fx_t ms;
     float tot;
-    group_lse<J>(M, S, &ms, &tot, term);
+    group_lse<J, G>(M, S, &ms, &tot, term);
     if (node && k == 0) {
       LV v;
       if (s == 0) {
@@ -412,11 +417,15 @@ __device__ void alpha_grouped(const Problem &p, const Workspace &ws, const Rings
   __syncthreads();
 }
 
-template <int ND>
+template <int ND, int G>
 __device__ void beta_grouped(const Problem &p, const Workspace &ws, const Rings<ND> &r,
                              long long b, int Tb, int Ub) {
-  constexpr int J = GroupArcs<ND>::J;
-  const int u = threadIdx.x / kGroup, k = threadIdx.x % kGroup;
+  constexpr int J = GroupArcs<ND, G>::J;
+  const int u = threadIdx.x / G, k = threadIdx.x % G;
+  // node index for ring reads: threads past the last row (u >= U+1, in the
+  // last warp) only join the barriers, and read row U1p - 1 so every read
+  // stays in bounds
+  const int uc = u < r.U1p ? u : r.U1p - 1;
   const int U1 = (int)p.U1;
   const fx_t *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * (2 * ND);
   LV *gbeta = ws.beta + b * p.n_diag * p.U1;
@@ -424,18 +433,18 @@ __device__ void beta_grouped(const Problem &p, const Workspace &ws, const Rings<
   int di[J], dd[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) {
-    di[j] = k + kGroup * j;
+    di[j] = k + G * j;
     dd[j] = di[j] < ND ? p.dur[di[j]] : -1;
   }
   const int last = Tb + Ub - 1;
-  for (int i = 0; i < kPrefetch; ++i) prefetch_group<ND>(gdiag0, r, last - i, u, k, Tb, Ub, U1);
+  for (int i = 0; i < kPrefetch; ++i) prefetch_group<ND, G>(gdiag0, r, last - i, u, k, Tb, Ub, U1);
   for (int q = last; q >= 0; --q) {
-    prefetch_group<ND>(gdiag0, r, q - kPrefetch, u, k, Tb, Ub, U1);
+    prefetch_group<ND, G>(gdiag0, r, q - kPrefetch, u, k, Tb, Ub, U1);
     cp_async_wait<kPrefetch>();
     __syncthreads();
     const int t = q - u;
     const bool node = u <= Ub && t >= 0 && t < Tb;
-    const fx_t *rec = r.w(q, u);
+    const fx_t *rec = r.w(q, uc);
     fx_t M[2 * J];
     float S[2 * J], term[2 * J];
 #pragma unroll
@@ -445,18 +454,18 @@ __device__ void beta_grouped(const Problem &p, const Workspace &ws, const Rings<
       // blank arc (t, u) -> (t+d, u), d > 0; the final blank lands on T_b
       const bool inb = node && d > 0 && t + d < Tb;
       const bool fin = node && d > 0 && t + d == Tb && u == Ub;
-      const LV bb = r.a(q + d, u);
+      const LV bb = r.a(q + d, uc);
       M[2 * j] = inb ? bb.m + rec[i] : (fin ? rec[i] : kFxVeryNeg);
       S[2 * j] = inb ? bb.s : (fin ? 1.0f : 0.0f);
       // label arc (t, u) -> (t+d, u+1)
       const bool okl = node && d >= 0 && u < Ub && t + d < Tb;
-      const LV bl = r.a(q + d + 1, u + 1 < r.U1p ? u + 1 : u);
+      const LV bl = r.a(q + d + 1, uc + 1 < r.U1p ? uc + 1 : uc);
       M[2 * j + 1] = okl ? bl.m + rec[ND + i] : kFxVeryNeg;
       S[2 * j + 1] = okl ? bl.s : 0.0f;
     }
     fx_t ms;
     float tot;
-    group_lse<J>(M, S, &ms, &tot, term);
+    group_lse<J, G>(M, S, &ms, &tot, term);
     const float inv = tot > 0.0f ? fast_rcp(tot) : 0.0f;
     float fb = 0.0f, fl = 0.0f;
     const long long n = (b * p.T + t) * p.U1 + u;
@@ -468,7 +477,7 @@ __device__ void beta_grouped(const Problem &p, const Workspace &ws, const Rings<
         ws.frac[(long long)(2 + di[j]) * nodes + n] = (term[2 * j] + term[2 * j + 1]) * inv;
     }
 #pragma unroll
-    for (int o = 1; o < kGroup; o <<= 1) {
+    for (int o = 1; o < G; o <<= 1) {
       fb += __shfl_xor_sync(0xffffffffu, fb, o);
       fl += __shfl_xor_sync(0xffffffffu, fl, o);
     }
@@ -492,8 +501,8 @@ __device__ void beta_grouped(const Problem &p, const Workspace &ws, const Rings<
   __syncthreads();
 }
 
-template <int ND>
-__global__ void __launch_bounds__(kLatticeMaxThreads)
+template <int ND, int G>
+__global__ void __launch_bounds__(kLatticeMaxThreads, 1)
 lattice_smem_kernel(Problem p, Workspace ws, long long b0, int RA, int RW) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const long long b = b0 + blockIdx.x;
@@ -503,17 +512,17 @@ lattice_smem_kernel(Problem p, Workspace ws, long long b0, int RA, int RW) {
   if (!is_beta && threadIdx.x == 0) write_utterance_info(p, ws, b, ok, sum_u);
   if (!ok) return;
   Rings<ND> r;
-  r.U1p = blockDim.x / kGroup;
+  r.U1p = (int)p.U1;
   r.mA = RA - 1;
   r.mW = RW - 1;
   r.A = reinterpret_cast<LV *>(smem_raw);
   r.W = reinterpret_cast<fx_t *>(r.A + RA * r.U1p);
   const int Tb = (int)p.logit_lens[b], Ub = (int)p.label_lens[b];
   if (!is_beta) {
-    alpha_grouped<ND>(p, ws, r, b, Tb, Ub);
+    alpha_grouped<ND, G>(p, ws, r, b, Tb, Ub);
     if (threadIdx.x == 0) termination(p, ws, b, Tb, Ub);
   } else {
-    beta_grouped<ND>(p, ws, r, b, Tb, Ub);
+    beta_grouped<ND, G>(p, ws, r, b, Tb, Ub);
   }
 }
 
@@ -531,10 +540,18 @@ int pow2_at_least(int v) {
 }
 
 // Shared bytes of the ring variant, or 0 when it does not apply.
+int group_width(const Problem &p) {
+  if (p.n_dur <= kGroupMax && p.U1 * kGroupMax <= kLatticeMaxThreads) return kGroupMax;
+  return 4;
+}
+
+// Shared bytes of the ring variant (or 0 when it does not apply); threads =
+// (U+1) * G rounded up to whole warps.
 size_t smem_plan(const Problem &p, int *RA, int *RW, int *threads) {
-  if (p.U1 * kGroup > kLatticeMaxThreads || p.n_dur > 9) return 0;
-  const int th = (int)(((p.U1 * kGroup + 31) / 32) * 32);
-  const int nodes_per_slot = th / kGroup;
+  const int G = group_width(p);
+  if (p.U1 * G > kLatticeMaxThreads || p.n_dur > 9) return 0;
+  const int th = (int)(((p.U1 * G + 31) / 32) * 32);
+  const int nodes_per_slot = (int)p.U1;
   const int ra = pow2_at_least(p.max_dur + 2);
   const int rw = pow2_at_least(kPrefetch + p.max_dur + 3);
   const size_t bytes =
@@ -546,14 +563,24 @@ size_t smem_plan(const Problem &p, int *RA, int *RW, int *threads) {
   return bytes;
 }
 
+template <int ND, int G>
+cudaError_t launch_smem_g(const Problem &p, const Workspace &ws, long long b0, dim3 grid, int th,
+                          size_t bytes, int RA, int RW, cudaStream_t stream) {
+  // at least kLatticeSmemFloor, so no node-table or gradient block shares the SM
+  if (bytes < (size_t)kLatticeSmemFloor) bytes = kLatticeSmemFloor;
+  cudaError_t e = cudaFuncSetAttribute(lattice_smem_kernel<ND, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  lattice_smem_kernel<ND, G><<<grid, th, bytes, stream>>>(p, ws, b0, RA, RW);
+  return cudaGetLastError();
+}
+
 template <int ND>
 cudaError_t launch_smem(const Problem &p, const Workspace &ws, long long b0, dim3 grid, int th,
                         size_t bytes, int RA, int RW, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(lattice_smem_kernel<ND>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e != cudaSuccess) return e;
-  lattice_smem_kernel<ND><<<grid, th, bytes, stream>>>(p, ws, b0, RA, RW);
-  return cudaGetLastError();
+  if (ND <= kGroupMax && group_width(p) == kGroupMax)
+    return launch_smem_g<ND, kGroupMax>(p, ws, b0, grid, th, bytes, RA, RW, stream);
+  return launch_smem_g<ND, 4>(p, ws, b0, grid, th, bytes, RA, RW, stream);
 }
 
 // ---------------------------------------------------------------- reduction

@@ -79,3 +79,15 @@ template <int DT> __device__ __forceinline__ int head_elems(const void *p) {
 }
 
 }  // namespace tdt
+
+namespace tdt {
+
+// Threads per row group for a row of row_bytes: the smallest power of two in
+// [8, 256] that covers the row with `batch` 16-byte loads per thread.
+inline int row_group_threads(long long row_bytes, int batch) {
+  int t = 8;
+  while (t < 256 && (long long)t * batch * 16 < row_bytes) t <<= 1;
+  return t;
+}
+
+}  // namespace tdt

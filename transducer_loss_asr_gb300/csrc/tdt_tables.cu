@@ -2,14 +2,17 @@
 //
 // "log-softmax over the vocabulary for each lattice node" ("tdt-loss: add
 // TDT loss kernel", kernels-community PR #882, "What's in it"), plus the
-// log-softmax of the duration logits.  One warp streams one logits row
-// z[b,t,u,0:V+D) once with 16-byte loads (scalar head/tail, see
-// tdt_rowio.cuh), keeping a running max and a running sum of exp(z - max)
-// per lane in fp32, then combines lanes with shuffles ("Warp Shuffle
-// Reductions", "cuda-kernels" skill page).  The row may be a slice of a
-// wider tensor: only strides s0..s2 locate it.  One warp per row and no grid
-// stride, so the blocks are short and other kernels can be scheduled
-// between them.
+// log-softmax of the duration logits.  A group of TPR threads streams one
+// logits row z[b,t,u,0:V+D) once: a scalar head up to the first 16-byte
+// boundary, a body of 16-byte loads (each thread issues kBatch independent
+// loads before touching any, so many bytes are in flight per SM), a scalar
+// tail (tdt_rowio.cuh).  Each thread keeps a running max and a running sum
+// of exp(z - max) in fp32; the group combines them with shuffles ("Warp
+// Shuffle Reductions", "cuda-kernels" skill page) and, for groups wider than
+// a warp, through shared memory.  TPR grows with the row length (8 threads
+// for rows of ~140 floats, a warp from ~2000 floats up), so the per-row
+// work is amortised over many vectors per thread.
+// The row may be a slice of a wider tensor: only strides s0..s2 locate it.
 //
 // Outputs per usable node (t < T_b, u <= U_b):
 //   lse_tok[n], lse_dur[n]   float, for the gradient pass
@@ -23,118 +26,182 @@ namespace tdt {
 namespace {
 
 constexpr int kTablesThreads = 256;
-constexpr int kTablesUnroll = 4;  // 16-byte vectors in flight per lane per iteration
+constexpr int kBatch = 8;          // 16-byte loads issued per thread before use
+constexpr int kVecPerThread = 16;  // row vectors per thread when choosing TPR
 
 __device__ __forceinline__ fx_t clamp_lp(fx_t v) {
   const fx_t floor_fx = (fx_t)kLogProbFloor * (fx_t)4294967296LL;
   return v < floor_fx ? floor_fx : v;
 }
 
-template <int DT>
+// Merge two (max, sum of exp(x - max)) pairs.
+__device__ __forceinline__ void merge_ms(float &m, float &s, float m2, float s2) {
+  const float M = fmaxf(m, m2);
+  if (M == -INFINITY) return;
+  s = s * fast_exp2((m - M) * kLog2e) + s2 * fast_exp2((m2 - M) * kLog2e);
+  m = M;
+}
+
+// Combine (m, s) over the TPR threads of each row group of the block.
+// Every thread of the block must call it (it may use __syncthreads).
+template <int TPR>
+__device__ __forceinline__ void group_ms(float &m, float &s, float *sm_m, float *sm_s) {
+  constexpr int W = TPR < 32 ? TPR : 32;
+#pragma unroll
+  for (int o = 1; o < W; o <<= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    merge_ms(m, s, m2, s2);
+  }
+  if (TPR > 32) {
+    constexpr int NW = TPR / 32;  // warps per group
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+      sm_m[warp] = m;
+      sm_s[warp] = s;
+    }
+    __syncthreads();
+    const int g0 = (warp / NW) * NW;
+    m = sm_m[g0];
+    s = sm_s[g0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) merge_ms(m, s, sm_m[g0 + w], sm_s[g0 + w]);
+    __syncthreads();
+  }
+}
+
+template <int DT, int TPR>
 __global__ void __launch_bounds__(kTablesThreads)
 node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) {
   typedef typename Elem<DT>::T E;
   constexpr int N = Vec<DT>::N;
+  constexpr int RPB = kTablesThreads / TPR;
+  __shared__ float sm_m[kTablesThreads / 32], sm_s[kTablesThreads / 32];
   const E *logits = static_cast<const E *>(p.logits);
-  const int lane = threadIdx.x & 31;
-  const long long n = n_begin + (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  if (n >= n_end) return;
-  const long long u = n % p.U1;
-  const long long bt = n / p.U1;
-  const long long t = bt % p.T;
-  const long long b = bt / p.T;
-  const long long Tb = p.logit_lens[b], Ub = p.label_lens[b];
-  if (Tb < 1 || Tb > p.T || Ub < 0 || Ub > p.U1 - 1) return;
-  if (t >= Tb || u > Ub) return;
+  const int lt = threadIdx.x % TPR;
+  const long long n = n_begin + (long long)blockIdx.x * RPB + threadIdx.x / TPR;
+  long long b = 0, t = 0, u = 0, Ub = 0;
+  bool active = n < n_end;
+  if (active) {
+    decode_node(p, n, &b, &t, &u);
+    const long long Tb = p.logit_lens[b];
+    Ub = p.label_lens[b];
+    active = Tb >= 1 && Tb <= p.T && Ub >= 0 && Ub <= p.U1 - 1 && t < Tb && u <= Ub;
+  }
   const E *row = logits + b * p.s0 + t * p.s1 + u * p.s2;
 
-  // token logits [0, V): scalar head and tail first, then 16-byte vectors
-  int head = head_elems<DT>(row);
-  if (head > p.V) head = (int)p.V;
-  const long long nvec = (p.V - head) / N;
-  const long long tail0 = head + nvec * N;
-  const int ntail = (int)(p.V - tail0);
+  // token logits [0, V)
   float m = -INFINITY, s = 0.0f;
-  if (lane < head) {
-    m = Elem<DT>::load(row + lane);
-    s = 1.0f;
-  } else if (lane < head + ntail) {
-    m = Elem<DT>::load(row + tail0 + (lane - head));
-    s = 1.0f;
-  }
-  // Two batches of kTablesUnroll 16-byte vectors per lane: the next batch is
-  // loaded before the math of the current one, so loads stay in flight.
-  const uint4 *vbase = reinterpret_cast<const uint4 *>(row + head);
-  const int nv = (int)nvec;
-  uint4 cur[kTablesUnroll], nxt[kTablesUnroll];
-#pragma unroll
-  for (int k = 0; k < kTablesUnroll; ++k) {
-    const int j = k * 32 + lane;
-    if (j < nv) cur[k] = __ldg(vbase + j);
-  }
-  for (int j0 = 0; j0 < nv; j0 += 32 * kTablesUnroll) {
-    const int jn = j0 + 32 * kTablesUnroll;
-#pragma unroll
-    for (int k = 0; k < kTablesUnroll; ++k) {
-      const int j = jn + k * 32 + lane;
-      if (j < nv) nxt[k] = __ldg(vbase + j);
+  if (active) {
+    int head = head_elems<DT>(row);
+    if (head > p.V) head = (int)p.V;
+    const int nvec = (int)((p.V - head) / N);
+    const int tail0 = head + nvec * N;
+    const int ntail = (int)(p.V - tail0);
+    // head (< N elements) and tail (< N elements) each on lanes 0.., TPR >= N
+    if (lt < head) {
+      m = Elem<DT>::load(row + lt);
+      s = 1.0f;
     }
-    float x[kTablesUnroll * N];
+    if (lt < ntail) merge_ms(m, s, Elem<DT>::load(row + tail0 + lt), 1.0f);
+    const uint4 *vbase = reinterpret_cast<const uint4 *>(row + head);
+    for (int j0 = 0; j0 < nvec; j0 += TPR * kBatch) {
+      uint4 v[kBatch];
 #pragma unroll
-    for (int k = 0; k < kTablesUnroll; ++k) {
-      if (j0 + k * 32 + lane < nv) {
-        unpack<DT>(cur[k], x + k * N);
-      } else {
+      for (int i = 0; i < kBatch; ++i) {
+        const int j = j0 + i * TPR + lt;
+        if (j < nvec) v[i] = __ldg(vbase + j);
+      }
+      float cm = -INFINITY;
 #pragma unroll
-        for (int e = 0; e < N; ++e) x[k * N + e] = -INFINITY;
+      for (int i = 0; i < kBatch; ++i) {
+        if (j0 + i * TPR + lt < nvec) {
+          float x[N];
+          unpack<DT>(v[i], x);
+#pragma unroll
+          for (int e = 0; e < N; ++e) cm = fmaxf(cm, x[e]);
+        }
+      }
+      if (cm > m) {
+        s *= fast_exp2((m - cm) * kLog2e);
+        m = cm;
+      }
+      if (m != -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+          if (j0 + i * TPR + lt < nvec) {
+            float x[N];
+            unpack<DT>(v[i], x);
+            // (x - m) first: exact for the terms near the max, which dominate
+#pragma unroll
+            for (int e = 0; e < N; ++e) s += fast_exp2((x[e] - m) * kLog2e);
+          }
+        }
       }
     }
-    float cm = x[0];
-#pragma unroll
-    for (int e = 1; e < kTablesUnroll * N; ++e) cm = fmaxf(cm, x[e]);
-    if (cm > m) {
-      s *= fast_exp2((m - cm) * kLog2e);
-      m = cm;
-    }
-    if (m != -INFINITY) {
-      // (x - m) first: exact for the terms near the max, which dominate the sum
-#pragma unroll
-      for (int e = 0; e < kTablesUnroll * N; ++e) s += fast_exp2((x[e] - m) * kLog2e);
-    }
-#pragma unroll
-    for (int k = 0; k < kTablesUnroll; ++k) cur[k] = nxt[k];
   }
-  const float M = warp_max(m);
-  const float S = warp_sum(m == -INFINITY ? 0.0f : s * fast_exp2((m - M) * kLog2e));
-  const fx_t lse_fx = fx_from_float(M) + fx_log_ge1(S);
+  group_ms<TPR>(m, s, sm_m, sm_s);
+  const float M = m, S = s;
 
-  // duration logits [V, V+D): one lane per duration
-  const float zd = (lane < p.D) ? Elem<DT>::load(row + p.V + lane) : -INFINITY;
-  const float Md = warp_max(zd);
-  const float Sd = warp_sum(lane < p.D ? fast_exp2((zd - Md) * kLog2e) : 0.0f);
-  const fx_t lsed_fx = fx_from_float(Md) + fx_log_ge1(Sd);
+  // duration logits [V, V+D): thread lt takes durations lt, lt+TPR, ...
+  float md = -INFINITY, sd = 0.0f;
+  if (active) {
+    for (int i = lt; i < p.D; i += TPR) {
+      const float z = Elem<DT>::load(row + p.V + i);
+      merge_ms(md, sd, z, 1.0f);
+    }
+  }
+  group_ms<TPR>(md, sd, sm_m, sm_s);
+  if (!active) return;
+  const fx_t lse_fx = fx_from_float(M) + fx_log_ge1(S);
+  const fx_t lsed_fx = fx_from_float(md) + fx_log_ge1(sd);
 
   // arc log-weights of this node: [i] blank arc with duration i, [D + i]
-  // label arc with duration i (lane i writes both)
-  fx_t wbs = 0, wls = 0;
-  if (lane == 0) {
-    const float zb = Elem<DT>::load(row + p.blank);
-    wbs = clamp_lp(fx_from_float(zb) - lse_fx) - p.sigma_fx;
-    if (u < Ub) {
-      const long long y = p.labels[b * (p.U1 - 1) + u];
-      if (y >= 0 && y < p.V && y != p.blank)
-        wls = clamp_lp(fx_from_float(Elem<DT>::load(row + y)) - lse_fx) - p.sigma_fx;
-    }
-    ws.lse_tok[n] = M + logf(S);
-    ws.lse_dur[n] = Md + logf(Sd);
+  // label arc with duration i
+  const float zb = Elem<DT>::load(row + p.blank);
+  const fx_t wbs = clamp_lp(fx_from_float(zb) - lse_fx) - p.sigma_fx;
+  fx_t wls = 0;
+  if (u < Ub) {
+    const long long y = p.labels[b * (p.U1 - 1) + u];
+    if (y >= 0 && y < p.V && y != p.blank)
+      wls = clamp_lp(fx_from_float(Elem<DT>::load(row + y)) - lse_fx) - p.sigma_fx;
   }
-  wbs = __shfl_sync(0xffffffffu, wbs, 0);
-  wls = __shfl_sync(0xffffffffu, wls, 0);
-  if (lane < p.D) {
-    const fx_t ld = clamp_lp(fx_from_float(zd) - lsed_fx);
-    fx_t *rec = ws.arcw + diag_index(p, b, t, u) * (2 * p.D);
-    rec[lane] = wbs + ld;
-    rec[p.D + lane] = wls + ld;
+  fx_t *rec = ws.arcw + diag_index(p, b, t, u) * (2 * p.D);
+  for (int i = lt; i < p.D; i += TPR) {
+    const fx_t ld = clamp_lp(fx_from_float(Elem<DT>::load(row + p.V + i)) - lsed_fx);
+    rec[i] = wbs + ld;
+    rec[p.D + i] = wls + ld;
+  }
+  if (lt == 0) {
+    ws.lse_tok[n] = M + logf(S);
+    ws.lse_dur[n] = md + logf(sd);
+  }
+}
+
+template <int DT, int TPR>
+cudaError_t launch_tpr(const Problem &p, const Workspace &ws, long long n_begin, long long n_end,
+                       cudaStream_t stream) {
+  constexpr int RPB = kTablesThreads / TPR;
+  const long long rows = n_end - n_begin;
+  const long long blocks = (rows + RPB - 1) / RPB;
+  node_tables_kernel<DT, TPR><<<(unsigned)blocks, kTablesThreads, kStreamSmemReserve, stream>>>(
+      p, ws, n_begin, n_end);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_dt(const Problem &p, const Workspace &ws, long long n_begin, long long n_end,
+                      cudaStream_t stream) {
+  // a warp per long row (no shared-memory combine), fewer lanes for short rows
+  int tpr = row_group_threads(p.V * (long long)sizeof(typename Elem<DT>::T), kVecPerThread);
+  if (tpr > 32) tpr = 32;
+  switch (tpr) {
+    case 8: return launch_tpr<DT, 8>(p, ws, n_begin, n_end, stream);
+    case 16: return launch_tpr<DT, 16>(p, ws, n_begin, n_end, stream);
+    case 32: return launch_tpr<DT, 32>(p, ws, n_begin, n_end, stream);
+    case 64: return launch_tpr<DT, 64>(p, ws, n_begin, n_end, stream);
+    case 128: return launch_tpr<DT, 128>(p, ws, n_begin, n_end, stream);
+    default: return launch_tpr<DT, 256>(p, ws, n_begin, n_end, stream);
   }
 }
 
@@ -142,17 +209,12 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
 
 cudaError_t launch_node_tables(const Problem &p, int dtype, const Workspace &ws,
                                long long n_begin, long long n_end, cudaStream_t stream) {
-  const long long rows = n_end - n_begin;
-  if (rows <= 0) return cudaSuccess;
-  const long long warps_per_block = kTablesThreads / 32;
-  const long long blocks = (rows + warps_per_block - 1) / warps_per_block;
-  dim3 grid((unsigned)blocks), block(kTablesThreads);
+  if (n_end - n_begin <= 0) return cudaSuccess;
   switch (dtype) {
-    case kF32: node_tables_kernel<kF32><<<grid, block, 0, stream>>>(p, ws, n_begin, n_end); break;
-    case kF16: node_tables_kernel<kF16><<<grid, block, 0, stream>>>(p, ws, n_begin, n_end); break;
-    default: node_tables_kernel<kBF16><<<grid, block, 0, stream>>>(p, ws, n_begin, n_end); break;
+    case kF32: return launch_dt<kF32>(p, ws, n_begin, n_end, stream);
+    case kF16: return launch_dt<kF16>(p, ws, n_begin, n_end, stream);
+    default: return launch_dt<kBF16>(p, ws, n_begin, n_end, stream);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace tdt
