@@ -41,9 +41,18 @@ METRIC = ("TDT loss fwd+bwd ms and achieved HBM GB/s (% of roofline) at "
 ELT = {"f32": 4, "f16": 2, "bf16": 2}
 FALLBACK_HBM_GBS = 6800.0
 
-# DRAM bytes (read + write) per launch of the dominant kernel from one ncu
-# capture, valid only while the kernel source has this sha256.
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) per launch of the gradient kernel from one ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum), valid only while
+# its sources hash to this sha256 (kernel_sha).
+NCU_TRAFFIC = {
+    # ncu --set full, one launch = one utterance [1,200,41,8198] fp32 (the
+    # per-launch work of the four-chunk B=4 bench): read 270059008 + written
+    # 209289728 bytes (the rest of the writes retire from L2 after the kernel)
+    ("grad", "parakeet"): {
+        "bytes": 270059008 + 209289728,
+        "sha256": "87e685a532848f9e188f93c753b806ba5645d5aa85822dd99ba5f1eec099ee4b",
+    },
+}
 
 
 def algorithmic_bytes(inp):
@@ -119,10 +128,16 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def source_sha(name):
-    p = os.path.join(ROOT, "transducer_loss_asr_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+KERNEL_SOURCES = {"grad": ("tdt_grad.cu", "tdt_rowio.cuh", "tdt_common.cuh")}
+
+
+def kernel_sha(kernel):
+    """sha256 over the sources a kernel is compiled from."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "transducer_loss_asr_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def oracle_sample(inp, max_utts=1, frames=None):
@@ -330,22 +345,30 @@ def main():
     e2e_value = world * step_bytes / (float(e2e_ms.item()) / 1e3) / 1e9
     assert torch.equal(loss_h, loss.cpu())
 
-    # roofline of the dominant kernel (live per-kernel events over the timed region)
+    # Roofline of the gradient pass (K4), the largest HBM-bound share of the
+    # step; the lattice passes are latency-bound, run on SMs of their own and
+    # overlap K1/K4 (their share is reported beside it).  Per-launch bytes are
+    # the step's algorithmic bytes over the K4 launches of one step.
     per_kernel = {k: {"ms_per_launch": (ms / n if n else 0.0), "launches": n}
                   for k, (ms, n) in kt.items()}
-    dom = max(kt, key=lambda k: kt[k][0])
-    ms_dom, n_dom = kt[dom]
-    kbytes = {"grad": read_b + write_b, "node_tables": read_b}
     peak, peak_kind = measured_peaks()
     roofline = None
-    if dom in kbytes and n_dom:
-        achieved = kbytes[dom] / (ms_dom / n_dom / 1e3) / 1e9
-        src = {"grad": "tdt_grad.cu", "node_tables": "tdt_tables.cu"}[dom]
-        tr = NCU_TRAFFIC.get((dom, w.name))
-        traffic = tr["bytes"] if tr and tr["sha256"] == source_sha(src) else None
-        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+    ms_g, n_g = kt.get("grad", (0.0, 0))
+    if n_g:
+        per_step = n_g / args.steps
+        bytes_launch = (read_b + write_b) / per_step
+        achieved = bytes_launch / (ms_g / n_g / 1e3) / 1e9
+        tr = NCU_TRAFFIC.get(("grad", w.name))
+        traffic = tr["bytes"] if tr and tr["sha256"] == kernel_sha("grad") else None
+        roofline = {"bound": "hbm", "kernel": "grad", "achieved": achieved, "peak": peak,
                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                    "algorithmic_bytes_per_launch": bytes_launch,
                     "peak_source": peak_kind + " hbm_gbs (copy)"}
+    ms_t, n_t = kt.get("node_tables", (0.0, 0))
+    if n_t:
+        per_kernel["node_tables"]["achieved_gbs"] = read_b * args.steps / (ms_t / 1e3) / 1e9
+    if n_g:
+        per_kernel["grad"]["achieved_gbs"] = roofline["achieved"]
     step_frac = (step_bytes / (ms_per_step / 1e3) / 1e9) / peak
 
     cpu = None

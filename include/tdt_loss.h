@@ -1,6 +1,6 @@
 /*
  * tdt_loss.h -- C ABI of the GB300 (sm_103a) Token-and-Duration Transducer
- * (TDT) loss: forward and backward in one call.
+ * (TDT) loss: forward and backward in one call, or split in two for autograd.
  *
  * The operation ("tdt-loss: add TDT loss kernel", kernels-community PR
  * #882, list "What's in it"):
@@ -44,6 +44,13 @@
  *               gradient of the reduced loss for an upstream gradient of 1
  *               (of sum_b L_b for NONE).  NULL computes the loss only.
  *               Rows outside an utterance's lattice are written as 0.
+ *               grad_out may be the logits pointer itself when the logits
+ *               are contiguous: the gradient then replaces the logits, so
+ *               no second [B,T,U+1,V+D] buffer is needed (a memory-lean
+ *               option; the pages report a lower training peak memory with
+ *               the fused kernel, "Fine-tune check": 33.6 -> 21.8 GiB).
+ *               Any other overlap of grad_out with the logits is rejected
+ *               with TDT_ERR_BAD_ALIASING.
  *   stream      a cudaStream_t (NULL: the legacy default stream).
  * Memory: the caller owns every pointer; the library never frees them.
  * Calls are asynchronous on `stream`: results are valid once the stream
@@ -94,6 +101,7 @@ extern "C" {
 #define TDT_ERR_CUDA (-10)
 #define TDT_ERR_BAD_ALIGNMENT (-11)
 #define TDT_ERR_NOALLOC_TOO_LARGE (-12)
+#define TDT_ERR_BAD_ALIASING (-13)
 
 /*
  * Loss and gradient in one call.  Internal scratch (per-node tables, alpha,
@@ -123,6 +131,38 @@ int tdt_loss_fwd_bwd_ws(const void *logits, const int64_t sizes[4], const int64_
                         const int64_t *label_lens, const int32_t *durations, int n_dur,
                         int blank, double sigma, int reduction, float *loss_out,
                         void *grad_out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The loss and its gradient in two calls, for autograd: the forward call
+ * computes the loss and keeps in `workspace` everything the gradient needs;
+ * the backward call, made later with the same arguments and the same
+ * workspace, writes the gradient for an upstream gradient `grad_loss`.
+ * The pages' layer supports backward and, through fake implementations of
+ * its ops, torch.compile ("Add TDT loss kernel", transformers PR #46048,
+ * review thread on the kernel mapping).
+ *
+ * tdt_loss_fwd: node tables, alpha, beta, per-row gradient coefficients and
+ *   the reduction into loss_out.  workspace as for tdt_loss_fwd_bwd_ws; its
+ *   contents must stay untouched until tdt_loss_bwd has run.
+ */
+int tdt_loss_fwd(const void *logits, const int64_t sizes[4], const int64_t strides[4], int dtype,
+                 const int64_t *labels, const int64_t *logit_lens, const int64_t *label_lens,
+                 const int32_t *durations, int n_dur, int blank, double sigma, int reduction,
+                 float *loss_out, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * tdt_loss_bwd: the gradient pass only.  grad_loss is the device float32
+ *   upstream gradient of loss_out ([B] for TDT_REDUCTION_NONE, else [1]) or
+ *   NULL for 1; grad_out[b,...] = grad_loss[b or 0] * dL/dz.  Every other
+ *   argument must equal the tdt_loss_fwd call's, and that call must come
+ *   before this one in stream order.  grad_out is required (may be the
+ *   logits themselves, see grad_out above).
+ */
+int tdt_loss_bwd(const void *logits, const int64_t sizes[4], const int64_t strides[4], int dtype,
+                 const int64_t *labels, const int64_t *logit_lens, const int64_t *label_lens,
+                 const int32_t *durations, int n_dur, int blank, double sigma, int reduction,
+                 const float *grad_loss, void *grad_out, const void *workspace,
+                 size_t workspace_bytes, void *stream);
 
 /*
  * Same loss and gradient as tdt_loss_fwd_bwd for callers that cannot

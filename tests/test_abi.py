@@ -33,7 +33,7 @@ def _declared_functions():
 def test_header_declares_entry_points():
     names = _declared_functions()
     for n in ("tdt_loss_fwd_bwd", "tdt_loss_fwd_bwd_ws", "tdt_loss_workspace_size",
-              "tdt_status_string", "tdt_loss_version"):
+              "tdt_loss_fwd", "tdt_loss_bwd", "tdt_status_string", "tdt_loss_version"):
         assert n in names
 
 
@@ -47,7 +47,7 @@ def test_library_exports_every_declared_symbol(lib):
 def test_version_and_status_strings(lib):
     assert lib.tdt_loss_version() == 1
     assert lib.tdt_status_string(0) == "ok"
-    for code in range(-11, 0):
+    for code in range(-13, 0):
         assert lib.tdt_status_string(code) != "unknown status"
     assert lib.tdt_status_string(-99) == "unknown status"
 
@@ -114,6 +114,8 @@ def _call(lib, **over):
     (dict(sigma=2000.0), -8),
     (dict(logits=FAKE + 2), -11),                # fp32 logits not 4-byte aligned
     (dict(grad_out=FAKE + 1, dtype=2), -11),
+    (dict(grad_out=FAKE + 4), -13),              # overlaps the logits, not in place
+    (dict(grad_out=FAKE, strides=[160, 32, 10, 1]), -13),  # in place over strided logits
 ])
 def test_host_validation_rejects(lib, over, code):
     assert _call(lib, **over) == code
@@ -146,3 +148,57 @@ def test_binding_rejects_bad_tensors(lib):
         lib.tdt_loss_fwd_bwd(z, None, None, None, [0, 1], 0)
     with pytest.raises(ValueError):
         lib.tdt_loss_fwd_bwd(torch.zeros(5, 3, 10), None, None, None, [0, 1], 0)
+
+
+def test_split_entry_points_validate(lib):
+    so = lib.lib
+    sizes = (ctypes.c_int64 * 4)(2, 5, 3, 10)
+    strides = (ctypes.c_int64 * 4)(150, 30, 10, 1)
+    durs = (ctypes.c_int32 * 3)(0, 1, 2)
+    need = lib.tdt_loss_workspace_size([2, 5, 3, 10], 3)
+    f = ctypes.c_void_p(FAKE)
+    head = [f, sizes, strides, 0, f, f, f, durs, 3, 6, 0.0, 4]
+    # forward: loss_out required, workspace checked
+    assert so.tdt_loss_fwd(*head, None, f, need, None) == -1
+    assert so.tdt_loss_fwd(*head, f, f, need - 1, None) == -9
+    assert so.tdt_loss_fwd(*head[:3], 9, *head[4:], f, f, need, None) == -4
+    # backward: grad_out required; grad_loss 4-byte aligned; workspace checked
+    assert so.tdt_loss_bwd(*head, f, None, f, need, None) == -1
+    assert so.tdt_loss_bwd(*head, ctypes.c_void_p(FAKE + 2), f, f, need, None) == -11
+    assert so.tdt_loss_bwd(*head, None, f, None, need, None) == -1
+    assert so.tdt_loss_bwd(*head, None, ctypes.c_void_p(FAKE + 4), f, need, None) == -13
+
+
+def test_autograd_workspace_formula_matches_library(lib):
+    from transducer_loss_asr_gb300.autograd import workspace_nbytes
+
+    rng = __import__("random").Random(5)
+    for _ in range(300):
+        B, T, U1, nd = rng.randint(0, 20), rng.randint(1, 3000), rng.randint(1, 1300), \
+            rng.randint(1, 32)
+        if T + U1 > 65536:
+            continue
+        assert int(workspace_nbytes(B, T, U1, nd)) == lib.tdt_loss_workspace_size(
+            [B, T, U1, nd + 5], nd)
+
+
+def test_autograd_op_fake_shapes_and_cpu_rejection(lib):
+    import torch
+
+    from transducer_loss_asr_gb300 import autograd
+
+    m = dict(device="meta")
+    z = torch.empty(2, 5, 3, 13, **m)
+    lab = torch.empty(2, 2, dtype=torch.long, **m)
+    lens = torch.empty(2, dtype=torch.long, **m)
+    for red, shape in (("mean", ()), ("none", (2,))):
+        loss, ws = torch.ops.tdt_gb300.tdt_loss_forward(z, lab, lens, lens, [0, 1, 2], 6, 0.0, red)
+        assert tuple(loss.shape) == shape and loss.dtype == torch.float32
+        assert ws.numel() == lib.tdt_loss_workspace_size([2, 5, 3, 13], 3)
+        g = torch.ops.tdt_gb300.tdt_loss_backward(loss, z, lab, lens, lens, ws, [0, 1, 2], 6,
+                                                  0.0, red)
+        assert g.shape == z.shape and g.dtype == z.dtype
+    # the ops have CUDA kernels only: no silent CPU path
+    with pytest.raises(NotImplementedError):
+        autograd.tdt_loss(torch.zeros(2, 5, 3, 13), torch.zeros(2, 2, dtype=torch.long),
+                          torch.full((2,), 5), torch.full((2,), 2), [0, 1, 2], 6)

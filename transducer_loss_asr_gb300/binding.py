@@ -44,6 +44,10 @@ def _load() -> ctypes.CDLL:
     lib.tdt_loss_fwd_bwd_ws.argtypes = common + [P, ctypes.c_size_t, P]
     lib.tdt_loss_fwd_bwd_noalloc.restype = I
     lib.tdt_loss_fwd_bwd_noalloc.argtypes = common + [P]
+    lib.tdt_loss_fwd.restype = I
+    lib.tdt_loss_fwd.argtypes = common[:-1] + [P, ctypes.c_size_t, P]
+    lib.tdt_loss_bwd.restype = I
+    lib.tdt_loss_bwd.argtypes = common[:-2] + [P, P, P, ctypes.c_size_t, P]
     lib.tdt_loss_workspace_size.restype = ctypes.c_size_t
     lib.tdt_loss_workspace_size.argtypes = [P, I]
     lib.tdt_status_string.restype = ctypes.c_char_p
@@ -86,14 +90,14 @@ def workspace_size(sizes, n_dur: int) -> int:
 
 
 def _marshal(logits, labels, logit_lens, label_lens, durations, blank, sigma, reduction,
-             loss_out, grad_out, compute_grad):
+             loss_out, grad_out, compute_grad, with_loss=True):
     if logits.dim() != 4:
         raise ValueError("logits must be [B, T, U+1, V+D]")
     if logits.dtype not in DTYPES:
         raise TypeError("logits dtype must be float32, float16 or bfloat16")
     B = logits.shape[0]
     dev = logits.device
-    if loss_out is None:
+    if loss_out is None and with_loss:
         loss_out = torch.empty(B if reduction == "none" else 1, dtype=torch.float32, device=dev)
     if compute_grad and grad_out is None:
         grad_out = torch.empty(logits.shape, dtype=logits.dtype, device=dev)
@@ -162,6 +166,53 @@ def tdt_loss_fwd_bwd_noalloc(logits, labels, logit_lens, label_lens, durations, 
     with torch.cuda.device(logits.device):
         _check(lib.tdt_loss_fwd_bwd_noalloc(*args, _stream_handle(logits.device)))
     return loss_out, grad_out
+
+
+def _new_workspace(logits, n_dur):
+    return torch.empty(max(1, workspace_size(logits.shape, n_dur)), dtype=torch.uint8,
+                       device=logits.device)
+
+
+def tdt_loss_fwd(logits, labels, logit_lens, label_lens, durations, blank, sigma=0.0,
+                 reduction="mean_volume", loss_out=None, workspace=None):
+    """Forward half of the split API: returns (loss, workspace).
+
+    The workspace (a uint8 CUDA tensor, created when not given) holds what
+    tdt_loss_bwd needs; keep it untouched until then.
+    """
+    args, loss_out, _ = _marshal(logits, labels, logit_lens, label_lens, durations, blank, sigma,
+                                 reduction, loss_out, None, False)
+    if workspace is None:
+        workspace = _new_workspace(logits, len(durations))
+    with torch.cuda.device(logits.device):
+        _check(lib.tdt_loss_fwd(*args[:-1], _ptr(workspace), workspace.numel(),
+                                _stream_handle(logits.device)))
+    return loss_out, workspace
+
+
+def tdt_loss_bwd(logits, labels, logit_lens, label_lens, durations, blank, workspace,
+                 grad_loss=None, sigma=0.0, reduction="mean_volume", grad_out=None):
+    """Backward half: the gradient for upstream gradient ``grad_loss``.
+
+    ``grad_loss``: float32 CUDA tensor with B elements ("none") or one
+    element, or None for 1.  Arguments other than grad_loss/grad_out must be
+    those of the tdt_loss_fwd call that filled ``workspace``.  ``grad_out``
+    may be ``logits`` itself (contiguous logits): the gradient then replaces
+    them.
+    """
+    B = logits.shape[0]
+    if grad_loss is not None:
+        want = B if reduction == "none" else 1
+        if (grad_loss.dtype != torch.float32 or not grad_loss.is_contiguous()
+                or grad_loss.numel() != want or grad_loss.device != logits.device):
+            raise ValueError("grad_loss must be a contiguous float32 tensor of %d element(s) "
+                             "on %s" % (want, logits.device))
+    args, _, grad_out = _marshal(logits, labels, logit_lens, label_lens, durations, blank, sigma,
+                                 reduction, None, grad_out, True, with_loss=False)
+    with torch.cuda.device(logits.device):
+        _check(lib.tdt_loss_bwd(*args[:-2], _ptr(grad_loss), args[-1], _ptr(workspace),
+                                workspace.numel(), _stream_handle(logits.device)))
+    return grad_out
 
 
 def tdt_loss_workspace_size(sizes, n_dur: int) -> int:

@@ -76,10 +76,11 @@ size_t elem_size(int dtype) { return dtype == TDT_DTYPE_F32 ? 4 : 2; }
 int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4], int dtype,
              const int64_t *labels, const int64_t *logit_lens, const int64_t *label_lens,
              const int32_t *durations, int n_dur, int blank, double sigma, int reduction,
-             const float *loss_out, const void *grad_out, Problem *p) {
+             const float *loss_out, const void *grad_out, Problem *p, bool need_loss) {
   if (!sizes || !strides || !durations) return TDT_ERR_NULL_POINTER;
   // loss_out may be NULL only when it has no elements (empty batch, reduction none)
-  if (!loss_out && !(sizes[0] == 0 && reduction == TDT_REDUCTION_NONE)) return TDT_ERR_NULL_POINTER;
+  if (need_loss && !loss_out && !(sizes[0] == 0 && reduction == TDT_REDUCTION_NONE))
+    return TDT_ERR_NULL_POINTER;
   if (dtype != TDT_DTYPE_F32 && dtype != TDT_DTYPE_F16 && dtype != TDT_DTYPE_BF16)
     return TDT_ERR_BAD_DTYPE;
   if (n_dur < 1 || n_dur > kMaxDurations) return TDT_ERR_BAD_DURATIONS;
@@ -107,6 +108,17 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
   if (((uintptr_t)logits % es) != 0 || (grad_out && ((uintptr_t)grad_out % es) != 0) ||
       ((uintptr_t)loss_out % 4) != 0)
     return TDT_ERR_BAD_ALIGNMENT;
+  // grad_out may overlap the logits only as the same contiguous tensor (the
+  // gradient written in place over the logits, row by row)
+  if (grad_out && B > 0) {
+    const long long span = ((B - 1) * strides[0] + (T - 1) * strides[1] + (U1 - 1) * strides[2] +
+                            VD) * (long long)es;
+    const long long gspan = B * T * U1 * VD * (long long)es;
+    const uintptr_t l0 = (uintptr_t)logits, g0 = (uintptr_t)grad_out;
+    const bool overlap = g0 < l0 + (uintptr_t)span && l0 < g0 + (uintptr_t)gspan;
+    const bool contiguous = strides[2] == VD && strides[1] == U1 * VD && strides[0] == T * U1 * VD;
+    if (overlap && !(g0 == l0 && contiguous)) return TDT_ERR_BAD_ALIASING;
+  }
 
   memset(p, 0, sizeof(*p));
   p->logits = logits;
@@ -212,14 +224,19 @@ DeviceRes *device_res(int dev) {
   return r;
 }
 
+// One loss (+ gradient) call.  coeffs: also run beta and the row
+// coefficients (always when grad_out is given; the forward half of the split
+// API keeps them for the backward half).  gscale: upstream gradient of the
+// loss (device, NULL = 1).
 int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void *grad_out,
-        cudaStream_t stream) {
+        const float *gscale, bool coeffs, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return TDT_ERR_CUDA;
   DeviceRes *res = device_res(dev);
   if (!res) return TDT_ERR_CUDA;
   std::lock_guard<std::mutex> g(res->mu);
   const bool with_grad = grad_out != nullptr;
+  coeffs = coeffs || with_grad;
   const long long rows_per_utt = p.T * p.U1;
   const int nchunk = (int)(p.B < kChunks ? (p.B > 0 ? p.B : 1) : kChunks);
   auto b_lo = [&](int c) { return p.B * c / nchunk; };
@@ -238,9 +255,8 @@ int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void 
     TDT_TRY(cudaEventRecord(res->tables_done[c], stream));
     TDT_TRY(cudaStreamWaitEvent(side, res->tables_done[c], 0));
     TDT_TRY(timed(TDT_KERNEL_LATTICE, side,
-                  [&] { return launch_lattice(p, ws, b0, b1, with_grad, side); }));
-    if (with_grad)
-      TDT_TRY(launch_row_coeffs(p, ws, b0 * rows_per_utt, b1 * rows_per_utt, side));
+                  [&] { return launch_lattice(p, ws, b0, b1, coeffs, side); }));
+    if (coeffs) TDT_TRY(launch_row_coeffs(p, ws, b0 * rows_per_utt, b1 * rows_per_utt, side));
     TDT_TRY(cudaEventRecord(res->lattice_done[c], side));
   }
   // the reduction needs every chunk's log-likelihood; it joins all side streams
@@ -253,12 +269,36 @@ int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void 
       const long long b0 = b_lo(c), b1 = b_lo(c + 1);
       TDT_TRY(cudaStreamWaitEvent(stream, res->lattice_done[c], 0));
       TDT_TRY(timed(TDT_KERNEL_GRAD, stream, [&] {
-        return launch_grad(p, dtype, ws, grad_out, b0 * rows_per_utt, b1 * rows_per_utt, stream);
+        return launch_grad(p, dtype, ws, grad_out, gscale, b0 * rows_per_utt, b1 * rows_per_utt,
+                           stream);
       }));
     }
   }
   TDT_TRY(cudaStreamWaitEvent(stream, res->join, 0));
 #undef TDT_TRY
+  return TDT_OK;
+}
+
+// The backward half of the split API: the gradient pass over every row.
+int run_bwd(const Problem &p, int dtype, const Workspace &ws, void *grad_out, const float *gscale,
+            cudaStream_t stream) {
+  if (p.B == 0) return TDT_OK;
+  if (timed(TDT_KERNEL_GRAD, stream, [&] {
+        return launch_grad(p, dtype, ws, grad_out, gscale, 0, p.B * p.T * p.U1, stream);
+      }) != cudaSuccess)
+    return TDT_ERR_CUDA;
+  return TDT_OK;
+}
+
+// Checks shared by the entry points that take caller-owned scratch.
+int check_workspace(const int64_t sizes[4], int n_dur, const void *workspace,
+                    size_t workspace_bytes, Workspace *ws) {
+  Layout L;
+  if (!make_layout(sizes, n_dur, &L)) return TDT_ERR_BAD_SIZES;
+  if (!workspace) return TDT_ERR_NULL_POINTER;
+  if (workspace_bytes < L.total) return TDT_ERR_WORKSPACE_TOO_SMALL;
+  if (((uintptr_t)workspace % 256) != 0) return TDT_ERR_BAD_ALIGNMENT;
+  *ws = carve(L, const_cast<void *>(workspace));
   return TDT_OK;
 }
 
@@ -280,15 +320,45 @@ int tdt_loss_fwd_bwd_ws(const void *logits, const int64_t sizes[4], const int64_
                         void *workspace, size_t workspace_bytes, void *stream) {
   tdt::Problem p;
   int rc = tdt::validate(logits, sizes, strides, dtype, labels, logit_lens, label_lens,
-                         durations, n_dur, blank, sigma, reduction, loss_out, grad_out, &p);
+                         durations, n_dur, blank, sigma, reduction, loss_out, grad_out, &p, true);
   if (rc != TDT_OK) return rc;
-  tdt::Layout L;
-  if (!tdt::make_layout(sizes, n_dur, &L)) return TDT_ERR_BAD_SIZES;
-  if (!workspace) return TDT_ERR_NULL_POINTER;
-  if (workspace_bytes < L.total) return TDT_ERR_WORKSPACE_TOO_SMALL;
-  if (((uintptr_t)workspace % 256) != 0) return TDT_ERR_BAD_ALIGNMENT;
-  tdt::Workspace ws = tdt::carve(L, workspace);
-  return tdt::run(p, dtype, ws, loss_out, grad_out, static_cast<cudaStream_t>(stream));
+  tdt::Workspace ws;
+  rc = tdt::check_workspace(sizes, n_dur, workspace, workspace_bytes, &ws);
+  if (rc != TDT_OK) return rc;
+  return tdt::run(p, dtype, ws, loss_out, grad_out, nullptr, false,
+                  static_cast<cudaStream_t>(stream));
+}
+
+int tdt_loss_fwd(const void *logits, const int64_t sizes[4], const int64_t strides[4], int dtype,
+                 const int64_t *labels, const int64_t *logit_lens, const int64_t *label_lens,
+                 const int32_t *durations, int n_dur, int blank, double sigma, int reduction,
+                 float *loss_out, void *workspace, size_t workspace_bytes, void *stream) {
+  tdt::Problem p;
+  int rc = tdt::validate(logits, sizes, strides, dtype, labels, logit_lens, label_lens,
+                         durations, n_dur, blank, sigma, reduction, loss_out, nullptr, &p, true);
+  if (rc != TDT_OK) return rc;
+  tdt::Workspace ws;
+  rc = tdt::check_workspace(sizes, n_dur, workspace, workspace_bytes, &ws);
+  if (rc != TDT_OK) return rc;
+  return tdt::run(p, dtype, ws, loss_out, nullptr, nullptr, true,
+                  static_cast<cudaStream_t>(stream));
+}
+
+int tdt_loss_bwd(const void *logits, const int64_t sizes[4], const int64_t strides[4], int dtype,
+                 const int64_t *labels, const int64_t *logit_lens, const int64_t *label_lens,
+                 const int32_t *durations, int n_dur, int blank, double sigma, int reduction,
+                 const float *grad_loss, void *grad_out, const void *workspace,
+                 size_t workspace_bytes, void *stream) {
+  tdt::Problem p;
+  if (!grad_out) return TDT_ERR_NULL_POINTER;
+  int rc = tdt::validate(logits, sizes, strides, dtype, labels, logit_lens, label_lens,
+                         durations, n_dur, blank, sigma, reduction, nullptr, grad_out, &p, false);
+  if (rc != TDT_OK) return rc;
+  if (((uintptr_t)grad_loss % 4) != 0) return TDT_ERR_BAD_ALIGNMENT;
+  tdt::Workspace ws;
+  rc = tdt::check_workspace(sizes, n_dur, workspace, workspace_bytes, &ws);
+  if (rc != TDT_OK) return rc;
+  return tdt::run_bwd(p, dtype, ws, grad_out, grad_loss, static_cast<cudaStream_t>(stream));
 }
 
 int tdt_loss_fwd_bwd(const void *logits, const int64_t sizes[4], const int64_t strides[4],
@@ -298,7 +368,7 @@ int tdt_loss_fwd_bwd(const void *logits, const int64_t sizes[4], const int64_t s
                      void *stream) {
   tdt::Problem p;
   int rc = tdt::validate(logits, sizes, strides, dtype, labels, logit_lens, label_lens,
-                         durations, n_dur, blank, sigma, reduction, loss_out, grad_out, &p);
+                         durations, n_dur, blank, sigma, reduction, loss_out, grad_out, &p, true);
   if (rc != TDT_OK) return rc;
   tdt::Layout L;
   if (!tdt::make_layout(sizes, n_dur, &L)) return TDT_ERR_BAD_SIZES;
@@ -306,7 +376,7 @@ int tdt_loss_fwd_bwd(const void *logits, const int64_t sizes[4], const int64_t s
   void *ws_ptr = nullptr;
   if (cudaMallocAsync(&ws_ptr, L.total, s) != cudaSuccess) return TDT_ERR_CUDA;
   tdt::Workspace ws = tdt::carve(L, ws_ptr);
-  rc = tdt::run(p, dtype, ws, loss_out, grad_out, s);
+  rc = tdt::run(p, dtype, ws, loss_out, grad_out, nullptr, false, s);
   if (cudaFreeAsync(ws_ptr, s) != cudaSuccess && rc == TDT_OK) rc = TDT_ERR_CUDA;
   return rc;
 }
@@ -326,6 +396,8 @@ const char *tdt_status_string(int status) {
     case TDT_ERR_WORKSPACE_TOO_SMALL: return "workspace smaller than tdt_loss_workspace_size";
     case TDT_ERR_CUDA: return "a CUDA call failed";
     case TDT_ERR_BAD_ALIGNMENT: return "a pointer is not aligned to its element size";
+    case TDT_ERR_BAD_ALIASING:
+      return "grad_out overlaps the logits other than as the same contiguous tensor";
     case TDT_ERR_NOALLOC_TOO_LARGE:
       return "problem needs more scratch than the fixed array of tdt_loss_fwd_bwd_noalloc "
              "(TDT_NOALLOC_MAX_WORKSPACE_BYTES); use tdt_loss_fwd_bwd or tdt_loss_fwd_bwd_ws";

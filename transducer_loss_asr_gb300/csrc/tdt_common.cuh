@@ -230,7 +230,7 @@ Workspace carve(const Layout &L, void *base);
 int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4], int dtype,
              const int64_t *labels, const int64_t *logit_lens, const int64_t *label_lens,
              const int32_t *durations, int n_dur, int blank, double sigma, int reduction,
-             const float *loss_out, const void *grad_out, Problem *p);
+             const float *loss_out, const void *grad_out, Problem *p, bool need_loss);
 
 // ---- launchers (one per translation unit) ----------------------------------
 // Rows are flat node ids n in [n_begin, n_end); utterances b in [b_begin, b_end).
@@ -240,8 +240,10 @@ cudaError_t launch_lattice(const Problem &p, const Workspace &ws, long long b_be
                            long long b_end, bool with_beta, cudaStream_t stream);
 cudaError_t launch_reduce(const Problem &p, const Workspace &ws, float *loss_out,
                           cudaStream_t stream);
+// gscale: device upstream gradient of the loss ([B] for kNone, else [1]) or NULL (= 1)
 cudaError_t launch_grad(const Problem &p, int dtype, const Workspace &ws, void *grad_out,
-                        long long n_begin, long long n_end, cudaStream_t stream);
+                        const float *gscale, long long n_begin, long long n_end,
+                        cudaStream_t stream);
 cudaError_t launch_row_coeffs(const Problem &p, const Workspace &ws, long long n_begin,
                               long long n_end, cudaStream_t stream);
 

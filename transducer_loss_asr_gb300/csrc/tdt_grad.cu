@@ -42,10 +42,10 @@ __device__ __forceinline__ void zero_row(typename Elem<DT>::T *out, long long VD
   for (int j = lt; j < nvec; j += TPR) v[j] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-template <int DT, int TPR>
+template <int DT, int TPR, bool COH>
 __global__ void __launch_bounds__(kGradThreads)
-grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, long long n_begin,
-            long long n_end) {
+grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gscale,
+            long long n_begin, long long n_end) {
   typedef typename Elem<DT>::T E;
   constexpr int N = Vec<DT>::N;
   constexpr int RPB = kGradThreads / TPR;
@@ -72,7 +72,7 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, long long n_beg
 #pragma unroll
     for (int i = 0; i < kBatch; ++i) {
       const int j = i * TPR + lt;
-      if (j < nvec) v[i] = __ldg(vin + j);
+      if (j < nvec) v[i] = ld_row16<COH>(vin + j);
     }
   }
   const float *rc = ws.rowc + n * p.rc_stride;
@@ -82,7 +82,9 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, long long n_beg
     zero_row<DT, TPR>(out, p.VD, lt);
     return;
   }
-  const float a = r0.x, lse2 = r0.y, lsed2 = r0.z, ab = r0.w, al = r1.x;
+  // upstream gradient of utterance b's loss (1 when none is given; x * 1 is exact)
+  const float gs = gscale ? gscale[p.reduction == kNone ? b : 0] : 1.0f;
+  const float a = r0.x * gs, lse2 = r0.y, lsed2 = r0.z, ab = r0.w * gs, al = r1.x * gs;
   const int y = __float_as_int(r1.y);
   auto g_at = [&](float x, long long k) {
     float g = a * fast_exp2(fmaf(x, kLog2e, -lse2));
@@ -94,10 +96,10 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, long long n_beg
   if (vec) {
     const long long tail0 = head + (long long)nvec * N;
     const int ntail = (int)(p.V - tail0);
-    if (lt < head) out[lt] = Elem<DT>::from_float(g_at(Elem<DT>::load(row + lt), lt));
+    if (lt < head) out[lt] = Elem<DT>::from_float(g_at(ld_elem<DT, COH>(row + lt), lt));
     if (lt < ntail) {
       const long long k = tail0 + lt;
-      out[k] = Elem<DT>::from_float(g_at(Elem<DT>::load(row + k), k));
+      out[k] = Elem<DT>::from_float(g_at(ld_elem<DT, COH>(row + k), k));
     }
     uint4 *vout = reinterpret_cast<uint4 *>(out + head);
     // vectors holding the two special entries (or -1)
@@ -109,7 +111,7 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, long long n_beg
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) {
           const int j = j0 + i * TPR + lt;
-          if (j < nvec) v[i] = __ldg(vin + j);
+          if (j < nvec) v[i] = ld_row16<COH>(vin + j);
         }
       }
 #pragma unroll
@@ -132,7 +134,7 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, long long n_beg
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
         const long long k = k0 + i * TPR + lt;
-        x[i] = (k < p.V) ? Elem<DT>::load(row + k) : 0.0f;
+        x[i] = (k < p.V) ? ld_elem<DT, COH>(row + k) : 0.0f;
       }
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
@@ -142,8 +144,9 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, long long n_beg
     }
   }
   for (int i = lt; i < p.D; i += TPR) {
-    const float zd = Elem<DT>::load(row + p.V + i);
-    out[p.V + i] = Elem<DT>::from_float(a * fast_exp2(fmaf(zd, kLog2e, -lsed2)) - rc[kRcD + i]);
+    const float zd = ld_elem<DT, COH>(row + p.V + i);
+    out[p.V + i] =
+        Elem<DT>::from_float(a * fast_exp2(fmaf(zd, kLog2e, -lsed2)) - rc[kRcD + i] * gs);
   }
 }
 
@@ -192,28 +195,39 @@ __global__ void row_coeff_kernel(Problem p, Workspace ws, long long n_begin, lon
 
 template <int DT, int TPR>
 cudaError_t launch_tpr(const Problem &p, const Workspace &ws, typename Elem<DT>::T *grad,
-                       long long n_begin, long long n_end, cudaStream_t stream) {
+                       const float *gscale, long long n_begin, long long n_end,
+                       cudaStream_t stream) {
   constexpr int RPB = kGradThreads / TPR;
   const long long rows = n_end - n_begin;
   const long long blocks = (rows + RPB - 1) / RPB;
-  grad_kernel<DT, TPR><<<(unsigned)blocks, kGradThreads, kStreamSmemReserve, stream>>>(
-      p, ws, grad, n_begin, n_end);
+  // the output overlaps the logits (written in place): coherent loads
+  const char *lo = static_cast<const char *>(p.logits);
+  const char *go = reinterpret_cast<const char *>(grad);
+  const long long span = (p.B - 1) * p.s0 + (p.T - 1) * p.s1 + (p.U1 - 1) * p.s2 + p.VD;
+  const bool overlap = p.B > 0 && go < lo + span * (long long)sizeof(*grad) &&
+                       lo < go + p.B * p.T * p.U1 * p.VD * (long long)sizeof(*grad);
+  if (overlap)
+    grad_kernel<DT, TPR, true><<<(unsigned)blocks, kGradThreads, kStreamSmemReserve, stream>>>(
+        p, ws, grad, gscale, n_begin, n_end);
+  else
+    grad_kernel<DT, TPR, false><<<(unsigned)blocks, kGradThreads, kStreamSmemReserve, stream>>>(
+        p, ws, grad, gscale, n_begin, n_end);
   return cudaGetLastError();
 }
 
 template <int DT>
-cudaError_t launch_dt(const Problem &p, const Workspace &ws, void *grad_out, long long n_begin,
-                      long long n_end, cudaStream_t stream) {
+cudaError_t launch_dt(const Problem &p, const Workspace &ws, void *grad_out, const float *gscale,
+                      long long n_begin, long long n_end, cudaStream_t stream) {
   typedef typename Elem<DT>::T E;
   E *g = static_cast<E *>(grad_out);
   const int tpr = row_group_threads(p.V * (long long)sizeof(E), kVecPerThread);
   switch (tpr) {
-    case 8: return launch_tpr<DT, 8>(p, ws, g, n_begin, n_end, stream);
-    case 16: return launch_tpr<DT, 16>(p, ws, g, n_begin, n_end, stream);
-    case 32: return launch_tpr<DT, 32>(p, ws, g, n_begin, n_end, stream);
-    case 64: return launch_tpr<DT, 64>(p, ws, g, n_begin, n_end, stream);
-    case 128: return launch_tpr<DT, 128>(p, ws, g, n_begin, n_end, stream);
-    default: return launch_tpr<DT, 256>(p, ws, g, n_begin, n_end, stream);
+    case 8: return launch_tpr<DT, 8>(p, ws, g, gscale, n_begin, n_end, stream);
+    case 16: return launch_tpr<DT, 16>(p, ws, g, gscale, n_begin, n_end, stream);
+    case 32: return launch_tpr<DT, 32>(p, ws, g, gscale, n_begin, n_end, stream);
+    case 64: return launch_tpr<DT, 64>(p, ws, g, gscale, n_begin, n_end, stream);
+    case 128: return launch_tpr<DT, 128>(p, ws, g, gscale, n_begin, n_end, stream);
+    default: return launch_tpr<DT, 256>(p, ws, g, gscale, n_begin, n_end, stream);
   }
 }
 
@@ -228,12 +242,13 @@ cudaError_t launch_row_coeffs(const Problem &p, const Workspace &ws, long long n
 }
 
 cudaError_t launch_grad(const Problem &p, int dtype, const Workspace &ws, void *grad_out,
-                        long long n_begin, long long n_end, cudaStream_t stream) {
+                        const float *gscale, long long n_begin, long long n_end,
+                        cudaStream_t stream) {
   if (n_end - n_begin <= 0) return cudaSuccess;
   switch (dtype) {
-    case kF32: return launch_dt<kF32>(p, ws, grad_out, n_begin, n_end, stream);
-    case kF16: return launch_dt<kF16>(p, ws, grad_out, n_begin, n_end, stream);
-    default: return launch_dt<kBF16>(p, ws, grad_out, n_begin, n_end, stream);
+    case kF32: return launch_dt<kF32>(p, ws, grad_out, gscale, n_begin, n_end, stream);
+    case kF16: return launch_dt<kF16>(p, ws, grad_out, gscale, n_begin, n_end, stream);
+    default: return launch_dt<kBF16>(p, ws, grad_out, gscale, n_begin, n_end, stream);
   }
 }
 

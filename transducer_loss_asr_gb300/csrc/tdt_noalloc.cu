@@ -68,7 +68,7 @@ extern "C" int tdt_loss_fwd_bwd_noalloc(const void *logits, const int64_t sizes[
                                         float *loss_out, void *grad_out, void *stream) {
   tdt::Problem p;
   int rc = tdt::validate(logits, sizes, strides, dtype, labels, logit_lens, label_lens,
-                         durations, n_dur, blank, sigma, reduction, loss_out, grad_out, &p);
+                         durations, n_dur, blank, sigma, reduction, loss_out, grad_out, &p, true);
   if (rc != TDT_OK) return rc;
   tdt::Layout L;
   if (!tdt::make_layout(sizes, n_dur, &L)) return TDT_ERR_BAD_SIZES;
@@ -83,7 +83,7 @@ extern "C" int tdt_loss_fwd_bwd_noalloc(const void *logits, const int64_t sizes[
   if (tdt::launch_lattice(p, ws, 0, p.B, with_grad, s) != cudaSuccess) return TDT_ERR_CUDA;
   if (with_grad && tdt::launch_row_coeffs(p, ws, 0, rows, s) != cudaSuccess) return TDT_ERR_CUDA;
   if (tdt::launch_reduce(p, ws, loss_out, s) != cudaSuccess) return TDT_ERR_CUDA;
-  if (with_grad && tdt::launch_grad(p, dtype, ws, grad_out, 0, rows, s) != cudaSuccess)
+  if (with_grad && tdt::launch_grad(p, dtype, ws, grad_out, nullptr, 0, rows, s) != cudaSuccess)
     return TDT_ERR_CUDA;
   return TDT_OK;
 }

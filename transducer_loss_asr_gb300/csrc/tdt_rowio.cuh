@@ -17,6 +17,30 @@ template <int DT> struct Vec {
   static constexpr int N = 16 / (int)sizeof(typename Elem<DT>::T);  // elements per vector
 };
 
+// 16-byte streaming load that does not allocate in L1 (each logits byte is
+// read once per pass).  With COH = false it takes the non-coherent read-only
+// path (the row is not written while the kernel runs); with COH = true a
+// plain global load, for the gradient pass writing over its own input.
+template <bool COH> __device__ __forceinline__ uint4 ld_row16(const uint4 *p) {
+  uint4 v;
+  if (COH)
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+  else
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+  return v;
+}
+
+// One element as float, read-only path unless COH.
+template <int DT, bool COH>
+__device__ __forceinline__ float ld_elem(const typename Elem<DT>::T *p) {
+  if (COH) return Elem<DT>::to_float(*p);
+  return Elem<DT>::load(p);
+}
+
 // Streaming 16-byte load through the read-only path.
 __device__ __forceinline__ uint4 ld_vec(const void *p) {
   return __ldg(reinterpret_cast<const uint4 *>(p));

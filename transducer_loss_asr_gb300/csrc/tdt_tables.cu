@@ -110,7 +110,7 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
         const int j = j0 + i * TPR + lt;
-        if (j < nvec) v[i] = __ldg(vbase + j);
+        if (j < nvec) v[i] = ld_row16<false>(vbase + j);
       }
       float cm = -INFINITY;
 #pragma unroll
