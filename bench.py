@@ -228,14 +228,26 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--batch", type=int, default=None,
                     help="override B (smaller profiling cases; not a bench line)")
+    ap.add_argument("--frames", type=int, default=None,
+                    help="override T (smaller profiling cases; not a bench line)")
+    ap.add_argument("--lattice-bands", type=int, default=0,
+                    help="force K row bands per utterance in the lattice passes (0: automatic)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = WORKLOADS[args.workload]
-    if args.batch is not None:
+    if args.batch is not None or args.frames is not None:
         from transducer_loss_asr_gb300.workloads import scaled
 
-        w = scaled(w, B=args.batch, name="%s_b%d" % (w.name, args.batch))
+        ch = {}
+        if args.batch is not None:
+            ch["B"] = args.batch
+        if args.frames is not None:
+            ch["T"] = args.frames
+            if w.T_range is not None:
+                ch["T_range"] = (min(w.T_range[0], args.frames), args.frames)
+        w = scaled(w, name="%s_%s" % (w.name, "_".join("%s%d" % (k, v) for k, v in ch.items()
+                                                         if k != "T_range")), **ch)
     if args.impl == "reference":
         return run_reference(args, w)
 
@@ -252,6 +264,7 @@ def main():
 
     from transducer_loss_asr_gb300 import binding
 
+    binding.tdt_loss_set_lattice_bands(args.lattice_bands)
     inp = make_inputs(w, device=dev, seed=w.seed + rank)
     logits = inp["logits"]
     read_b, write_b, valid_rows, all_rows = algorithmic_bytes(inp)

@@ -218,6 +218,16 @@ void tdt_loss_timing_enable(int on);
  */
 int tdt_loss_timing_read(double *ms_out, int64_t *count_out, int n, int reset);
 
+/*
+ * Tuning and testing support.  The lattice passes split an utterance's rows
+ * u into K bands, one CTA each, in a thread-block cluster (K <= 16).
+ * bands > 0 forces K = min(bands, 16) for later calls (fewer when such a
+ * cluster does not fit the GPU); 0 restores the per-problem choice.  The
+ * results do not depend on K, bit for bit.  Process-wide; returns the
+ * previous setting.
+ */
+int tdt_loss_set_lattice_bands(int bands);
+
 /* Human-readable text for a status code (static storage). */
 const char *tdt_status_string(int status);
 

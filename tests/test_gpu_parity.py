@@ -263,3 +263,39 @@ def test_full_size_sampled(binding, oracle_mod, name):
     tol = 1e-4 if w.dtype == "f32" else 5e-2
     assert rs[:, : w.V].sum(-1).abs().max().item() <= tol
     assert rs[:, w.V:].sum(-1).abs().max().item() <= tol
+
+
+# ------------------------------------------------------------- lattice bands
+
+BANDED = {
+    "d5_ragged": dict(B=3, T=37, U=40, V=100, blank=99, durations=(0, 1, 2, 3, 4), dtype="f32",
+                      std=1.0, sigma=0.05, reduction="mean_volume", T_range=(20, 37),
+                      U_range=(25, 40)),
+    "d9_long": dict(B=2, T=60, U=70, V=50, blank=49, durations=tuple(range(9)), dtype="f32",
+                    std=1.0, sigma=0.02, reduction="none"),
+    "d3_no_zero": dict(B=2, T=45, U=33, V=40, blank=0, durations=(1, 2, 4), dtype="bf16",
+                       std=1.5, sigma=0.0, reduction="sum", T_range=(30, 45), U_range=(5, 33)),
+}
+
+
+@pytest.mark.parametrize("name", sorted(BANDED))
+def test_lattice_bands_do_not_change_results(binding, oracle_mod, name):
+    """The lattice rows are split into K bands (one CTA each, a thread-block
+    cluster); the arithmetic per node is the same for every K, so the loss and
+    the gradient must agree bit for bit, and with the oracle."""
+    w = scaled(WORKLOADS["tiny"], name="bands_" + name, seed=4242, **BANDED[name])
+    inp = make_inputs(w, device="cuda")
+    results = []
+    for K in (0, 1, 2, 3, 7, 16):
+        prev = binding.tdt_loss_set_lattice_bands(K)
+        try:
+            loss, grad = run_gpu(binding, inp)
+        finally:
+            binding.tdt_loss_set_lattice_bands(prev)
+        results.append((K, loss.clone(), grad.clone()))
+    for K, loss, grad in results[1:]:
+        assert torch.equal(loss, results[0][1]), "loss differs with %d bands" % K
+        assert torch.equal(grad, results[0][2]), "grad differs with %d bands" % K
+    ref = run_oracle(oracle_mod, inp)
+    check_loss(results[0][1], ref.loss, w.dtype)
+    check_grad(results[0][2], ref.grad, w.dtype)

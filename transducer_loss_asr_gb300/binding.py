@@ -54,6 +54,8 @@ def _load() -> ctypes.CDLL:
     lib.tdt_status_string.argtypes = [I]
     lib.tdt_loss_version.restype = I
     lib.tdt_loss_version.argtypes = []
+    lib.tdt_loss_set_lattice_bands.restype = I
+    lib.tdt_loss_set_lattice_bands.argtypes = [I]
     lib.tdt_loss_timing_enable.restype = None
     lib.tdt_loss_timing_enable.argtypes = [I]
     lib.tdt_loss_timing_read.restype = I
@@ -226,6 +228,12 @@ def tdt_status_string(status: int) -> str:
 
 def tdt_loss_version() -> int:
     return int(lib.tdt_loss_version())
+
+
+def tdt_loss_set_lattice_bands(bands: int) -> int:
+    """Force K bands (CTAs per utterance and direction) in the lattice passes;
+    0 = automatic.  Results do not depend on K.  Returns the previous value."""
+    return int(lib.tdt_loss_set_lattice_bands(int(bands)))
 
 
 KERNEL_NAMES = ("node_tables", "lattice", "unused", "reduce", "grad")

@@ -40,7 +40,7 @@ bool make_layout(const int64_t sizes[4], int n_dur, Layout *L) {
     off = align_up(off + bytes);
     return at;
   };
-  L->arcw = take(ndiag * 8 * 2 * (size_t)n_dur);
+  L->arcw = take(ndiag * 8 * (size_t)arc_record_len(n_dur));
   L->alpha = take(ndiag * sizeof(LV));
   L->beta = take(ndiag * sizeof(LV));
   L->lse_tok = take(nodes * 4);
@@ -135,6 +135,7 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
   p->sigma_fx = (fx_t)llround(sigma * kFxOne);
   p->n_diag = T + U1 - 1;
   p->rc_stride = row_coeff_stride(n_dur);
+  p->rec_len = arc_record_len(n_dur);
   return TDT_OK;
 }
 

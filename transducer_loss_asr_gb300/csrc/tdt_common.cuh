@@ -58,7 +58,15 @@ struct Problem {
   fx_t sigma_fx;
   long long n_diag;               // T + U1 - 1 anti-diagonals per utterance
   int rc_stride;                  // floats per row-coefficient record
+  int rec_len;                    // fx values per node arc record (arc_record_len)
 };
+
+// Node arc record (fx values), one per lattice node in anti-diagonal order:
+//   [i] = lpB - sigma + lpD_i      blank arc with duration i
+//   [D + i] = lpL - sigma + lpD_i  label arc with duration i (lpL taken as 0
+//                                  where no label arc leaves the node)
+// so a lattice pass adds one value per arc; 2D values = a 16-byte multiple.
+__host__ __device__ inline int arc_record_len(int n_dur) { return 2 * n_dur; }
 
 // Row-coefficient record (floats) the gradient pass reads for node n:
 enum RowCoeff {
@@ -72,8 +80,8 @@ enum RowCoeff {
   kRcD = 8,      // [kRcD + i] = c_b N fD_i
 };
 // Shared memory a K1/K4 block reserves without using it: with it, no K1/K4
-// block fits beside a lattice block (which requests kLatticeSmemFloor), so
-// the latency-bound lattice passes get SMs of their own.
+// block fits beside a lattice block (which requests at least
+// kLatticeSmemFloor), so the latency-bound lattice passes get SMs of their own.
 constexpr int kStreamSmemReserve = 32 * 1024;
 constexpr int kLatticeSmemFloor = 200 * 1024;
 
@@ -88,9 +96,7 @@ struct __align__(16) LV {
 // Scratch layout (device pointers carved from one workspace block).
 struct Workspace {
   // anti-diagonal-major, node index g = (b * n_diag + t + u) * U1 + u
-  fx_t *arcw;    // [g][2D] arc log-weights of node g: [i] blank arc with
-                 //   duration i: lpB - sigma + lpD_i; [D + i] label arc with
-                 //   duration i: lpL - sigma + lpD_i (unused at u = U_b)
+  fx_t *arcw;    // [g][rec_len] node arc records (arc_record_len)
   LV *alpha;     // [g]
   LV *beta;      // [g]
   // node-major per-row data, index n = (b * T + t) * U1 + u

@@ -4,34 +4,49 @@
 // long label sequences, no 1024-label limit)" ("tdt-loss: add TDT loss
 // kernel", kernels-community PR #882, "What's in it").  alpha(t,u) depends on
 // (t-d,u) for d > 0 and on (t-d,u-1) for every d including 0, so all of its
-// inputs lie on earlier anti-diagonals t+u: one CTA per utterance and
-// direction walks the anti-diagonals (in reverse for beta), one thread per
-// node of the current diagonal, one barrier per diagonal.  Values are
-// (m, s) pairs (tdt_common.cuh): exact 64-bit fixed point m plus an fp32
+// inputs lie on earlier anti-diagonals t+u: the passes walk the
+// anti-diagonals (in reverse for beta), one barrier per diagonal.  Values
+// are (m, s) pairs (tdt_common.cuh): exact 64-bit fixed point m plus an fp32
 // mantissa s in [1, 2).  alpha and beta are also stored in global memory in
 // the anti-diagonal layout for the gradient pass.
 //
 // Two variants:
-//  * lattice_smem_kernel (U+1 <= 256, D <= 9, rings <= 200 KB): thread u
-//    owns lattice row u; alpha/beta of the last RA diagonals sit in a shared
-//    ring of 16-byte (m, s) records, and the arc-weight records of the
+//  * lattice_cluster_kernel (D <= 9): the rows u of an utterance's lattice
+//    are split into K bands, one CTA each, the K CTAs of an utterance and
+//    direction forming a thread-block cluster.  G lanes serve one node (lane
+//    k takes durations k, k+G, ...).  A CTA keeps the values of the last RA
+//    diagonals of its rows in a shared ring, and the arc records of the
 //    diagonals in flight in a second ring that cp.async fills kPrefetch
 //    diagonals ahead, so no global round trip sits on the diagonal-to-
-//    diagonal critical path.  Templated on the exact number of durations so
-//    the arc loop is fully unrolled; all index arithmetic is 32-bit.
+//    diagonal path.  K is the fewest bands whose rings fit one CTA: a
+//    diagonal step is latency-bound, so splitting rows does not shorten it.
+//    With K = 1 (U+1 up to ~128) the kernel is compiled without any exchange.
+//    With K > 1 the one row a band needs from its neighbour (u_lo - 1 for
+//    alpha, u_hi + 1 for beta) is pushed into the neighbour's ring through
+//    distributed shared memory after every diagonal (st.async counted on an
+//    mbarrier per ring slot), and a second mbarrier per slot says "consumed",
+//    so neighbouring bands run a few diagonals apart with no cluster-wide
+//    barrier per diagonal.  Every wait is bounded: past the limit the
+//    utterance is marked unusable (NaN loss) and the CTA stops.
 //  * alpha_kernel / beta_kernel: the same wavefront reading and writing
 //    global memory, any U and D (no limit on label length).
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "tdt_common.cuh"
 
 namespace tdt {
 
+extern __shared__ __align__(16) unsigned char tdt_dyn_smem[];
+
+// Band count forced by tdt_loss_set_lattice_bands (0: chosen per problem).
+std::atomic<int> g_forced_bands{0};
+
 namespace {
 
 constexpr int kLatticeMaxThreads = 1024;
-constexpr int kPrefetch = 6;
-// Lanes per lattice node in the grouped shared-ring variant: 8 when a
-// node's durations fit one per lane and the block fits, else 4.
-constexpr int kGroupMax = 8;
 
 __device__ __forceinline__ fx_t fmax_fx(fx_t a, fx_t b) { return a > b ? a : b; }
 
@@ -158,8 +173,9 @@ __device__ void termination(const Problem &p, const Workspace &ws, long long b, 
     if (d <= 0 || Tb - d < 0) continue;
     const long long g = diag_index(p, b, Tb - d, Ub);
     const LV a = ws.alpha[g];
+    const fx_t *rec = ws.arcw + g * p.rec_len;
     S[i] = a.s;
-    if (a.s > 0.0f) M[i] = a.m + ws.arcw[g * (2 * p.n_dur) + i];
+    if (a.s > 0.0f) M[i] = a.m + rec[i];
   }
   fx_t m;
   float s;
@@ -212,14 +228,16 @@ alpha_kernel(Problem p, Workspace ws, long long b0) {
           if (d > 0) {
             const long long g = diag_index(p, b, t - d, u);
             const LV a = ws.alpha[g];
+            const fx_t *rec = ws.arcw + g * p.rec_len;
             S[i] = a.s;
-            if (a.s > 0.0f) M[i] = a.m + ws.arcw[g * (2 * nd) + i];
+            if (a.s > 0.0f) M[i] = a.m + rec[i];
           }
           if (u >= 1) {
             const long long g = diag_index(p, b, t - d, u - 1);
             const LV a = ws.alpha[g];
+            const fx_t *rec = ws.arcw + g * p.rec_len;
             S[nd + i] = a.s;
-            if (a.s > 0.0f) M[nd + i] = a.m + ws.arcw[g * (2 * nd) + nd + i];
+            if (a.s > 0.0f) M[nd + i] = a.m + rec[nd + i];
           }
         }
         lse_combine_n(M, S, 2 * nd, &m, &sv, nullptr, nullptr);
@@ -245,7 +263,7 @@ beta_kernel(Problem p, Workspace ws, long long b0) {
     for (long long u = u_lo + threadIdx.x; u <= u_hi; u += blockDim.x) {
       const long long t = s - u;
       const long long q = diag_index(p, b, t, u);
-      const fx_t *rec = ws.arcw + q * (2 * nd);
+      const fx_t *rec = ws.arcw + q * p.rec_len;
       fx_t M[2 * kMaxDurations];
       float S[2 * kMaxDurations], term[2 * kMaxDurations];
       for (int i = 0; i < nd; ++i) {
@@ -278,7 +296,7 @@ beta_kernel(Problem p, Workspace ws, long long b0) {
   }
 }
 
-// ---------------------------------------------------------------- shared-ring variant
+// ---------------------------------------------------------------- cluster variant
 
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
@@ -288,78 +306,222 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N> __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
+// Diagonals of arc records copied ahead of use: at ~0.5-1 us per diagonal
+// this covers the L2/HBM latency several times over.
+constexpr int kPrefetch = 4;
 
-// Shared rings of one CTA: A[RA][U1p] lattice values of the last RA
-// diagonals; W[RW][U1p][2 ND] arc-weight records of the diagonals in flight.
-template <int ND> struct Rings {
-  LV *A;
-  fx_t *W;
-  int mA, mW, U1p;
-  __device__ __forceinline__ LV &a(int q, int u) const { return A[(q & mA) * U1p + u]; }
-  __device__ __forceinline__ const fx_t *w(int q, int u) const {
-    return W + ((q & mW) * U1p + u) * (2 * ND);
+// ---- cluster / mbarrier primitives (PTX ISA: mbarrier, mapa, barrier.cluster)
+__device__ __forceinline__ unsigned smem_u32(const void *p) {
+  return (unsigned)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+__device__ __forceinline__ void mbar_init(unsigned long long *bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init_cluster() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Shared-memory address, in CTA `cta` of the cluster, of the local object at p.
+__device__ __forceinline__ unsigned map_cta(const void *p, unsigned cta) {
+  unsigned r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(cta));
+  return r;
+}
+// Asynchronous 16-byte store into another CTA's shared memory that, when the
+// bytes land, counts them on that CTA's mbarrier (complete_tx): no release
+// fence, so the storing thread never waits for its own earlier memory traffic.
+__device__ __forceinline__ void st_async_lv(unsigned addr, const LV &v, unsigned bar_addr) {
+  const unsigned long long m = (unsigned long long)v.m;
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
+      ::"r"(addr), "r"((unsigned)(m & 0xffffffffull)), "r"((unsigned)(m >> 32)),
+      "r"(__float_as_uint(v.s)), "r"(__float_as_uint(v.pad)), "r"(bar_addr)
+      : "memory");
+}
+// Arrive on a local mbarrier and expect `bytes` more transaction bytes this phase.
+__device__ __forceinline__ void arrive_expect_tx(unsigned long long *bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster, relaxed: used only
+// to say "slot consumed", after a CTA barrier that every reader of the slot
+// reached with its loads of the slot already returned (their values feed
+// the selects before the group shuffles), so no later store into the slot can
+// affect them; a release here would be a cluster-scope fence per step.
+__device__ __forceinline__ void arrive_cluster_relaxed(unsigned bar_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr)
+               : "memory");
+}
+// Non-blocking probe of a phase (test_wait never suspends the thread, so a
+// completion signalled from another SM is seen at the next probe).
+__device__ __forceinline__ bool test_wait_parity(unsigned long long *bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// About one second at the GB300 clock: far beyond any legitimate wait.
+constexpr long long kWaitLimitCycles = 2000000000LL;
+// Wait for the completion of the phase of parity `parity`; false on timeout.
+__device__ __forceinline__ bool wait_parity_bounded(unsigned long long *bar, unsigned parity) {
+  if (test_wait_parity(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!test_wait_parity(bar, parity))
+    if (clock64() - t0 > kWaitLimitCycles) return false;
+  return true;
+}
+
+// Lanes per node: one per duration up to 8 (a power of two, so a node's
+// lanes are an aligned part of a warp); 4 lanes of 3 durations for D = 9.
+constexpr int group_lanes(int nd) { return nd <= 1 ? 1 : nd <= 2 ? 2 : nd <= 4 ? 4 : nd <= 8 ? 8 : 4; }
+
+// Launch-time shape of the cluster variant.
+struct ClusterPlan {
+  int K;        // CTAs per (utterance, direction): the cluster size
+  int Rc;       // lattice rows per CTA
+  int G;        // lanes per node
+  int RA, RW;   // slots of the value ring and of the record ring (powers of two)
+  int threads;  // (Rc + 1) * G rounded up to whole warps, plus a control warp if K > 1
+  size_t smem;  // shared bytes used
+};
+
+// Shared memory of one CTA (dynamic shared memory, addressed by byte offset
+// from tdt_dyn_smem so every ring access is a 32-bit shared-space access):
+//   A[RA][Rc + 2]  LV   ring row r holds lattice row u_lo + r - 1: r = 0 is
+//                       the row below the band (alpha's halo), r = Rc + 1 the
+//                       row above it (beta's halo)
+//   W[RW][Rc + 1][REC]  node arc records of rows u_lo - 1 .. u_lo + Rc - 1
+//   full[RA], empty[RA] mbarriers of the halo slots
+template <int REC> struct ClusterRings {
+  unsigned offW, offBar;  // byte offsets of W and of full[] (empty[] follows)
+  int mA, mW, RA, slotA, slotW;  // masks, slot count, bytes per slot
+  __device__ __forceinline__ LV &a(int q, int r) const {
+    return *reinterpret_cast<LV *>(tdt_dyn_smem + (q & mA) * slotA + r * (int)sizeof(LV));
+  }
+  __device__ __forceinline__ const fx_t *w(int q, int r) const {
+    return reinterpret_cast<const fx_t *>(tdt_dyn_smem + offW + (q & mW) * slotW + r * (REC * 8));
+  }
+  __device__ __forceinline__ fx_t *w_mut(int q, int r) const {
+    return reinterpret_cast<fx_t *>(tdt_dyn_smem + offW + (q & mW) * slotW + r * (REC * 8));
+  }
+  __device__ __forceinline__ unsigned long long *full(int i) const {
+    return reinterpret_cast<unsigned long long *>(tdt_dyn_smem + offBar) + i;
+  }
+  __device__ __forceinline__ unsigned long long *empty(int i) const {
+    return reinterpret_cast<unsigned long long *>(tdt_dyn_smem + offBar) + RA + i;
   }
 };
 
-// Start the copies of diagonal q's record of node u (if it is a lattice
-// node): lane k of the group copies the 16-byte chunks k, k+G, ...; every
-// lane commits one group per call so the group count per step is fixed.
-template <int ND, int G>
-__device__ __forceinline__ void prefetch_group(const fx_t *gdiag0, const Rings<ND> &r, int q,
-                                               int u, int k, int Tb, int Ub, int U1) {
+size_t cluster_smem_bytes(int RA, int RW, int Rc, int rec) {
+  return (size_t)RA * (Rc + 2) * sizeof(LV) + (size_t)RW * (Rc + 1) * rec * 8 + 2 * (size_t)RA * 8;
+}
+
+// Copy diagonal q's record of lattice row u (if it is a lattice node) into
+// the record ring: lane k copies the 16-byte chunks k, k+G, ...; every lane
+// commits one group per call so the group count per step is uniform.
+template <int REC, int G>
+__device__ __forceinline__ void prefetch_rec(const fx_t *gdiag0, const ClusterRings<REC> &r,
+                                             int q, int u, int ring_row, int k, int Tb, int Ub,
+                                             int U1, bool want) {
   const int t = q - u;
-  if (q >= 0 && u <= Ub && t >= 0 && t < Tb) {
-    const fx_t *src = gdiag0 + ((long long)q * U1 + u) * (2 * ND);
-    fx_t *dst = r.W + ((q & r.mW) * r.U1p + u) * (2 * ND);
-    for (int c = k; c < ND; c += G) cp_async16(dst + 2 * c, src + 2 * c);
+  if (want && q >= 0 && u >= 0 && u <= Ub && t >= 0 && t < Tb) {
+    const fx_t *src = gdiag0 + ((long long)q * U1 + u) * REC;
+    fx_t *dst = r.w_mut(q, ring_row);
+    for (int c = k; c < REC / 2; c += G) cp_async16(dst + 2 * c, src + 2 * c);
   }
   cp_async_commit();
 }
 
-// Grouped variant: lane k of a node's group of G lanes handles
-// durations k, k+G, ... (both the blank and the label arc of each), so every
-// lane runs the same instructions; the int64 max and the fp32 sum are
-// combined across the group with xor shuffles.
-
-template <int ND, int G>
-struct GroupArcs {
-  static constexpr int J = (ND + G - 1) / G;  // durations per lane
-};
-
-// Group-wide log-sum-exp of this lane's 2J candidates; returns the group's
-// M* and S (S = 0 when the group has no finite candidate) and each
+// Group-wide log-sum-exp of this lane's 2J candidates (M_j, S_j).  The
+// reference R is the group's largest integer part, floor(M_j) (the high word
+// of the fx value): a 32-bit max, one shuffle per round, exact, and at most
+// one natural unit below the true maximum, so every term S_j e^(M_j - R) is
+// below 2e and the largest is >= 1.  M_j - R = (hi_j - hmax) + lo_j 2^-32 is
+// converted with the integer difference taken first, so terms near the
+// maximum carry only fp32 rounding of numbers below 1.  Returns R, the sum S
+// (0 when no candidate is finite: the masked ones have S_j = 0) and each
 // candidate's unnormalised term.
 template <int J, int G>
-__device__ __forceinline__ void group_lse(const fx_t *M, const float *S, fx_t *ms_out,
+__device__ __forceinline__ void group_lse(const fx_t *M, const float *S, fx_t *ref_out,
                                           float *tot_out, float *term) {
-  fx_t ms = M[0];
+  int hmax = (int)(M[0] >> 32);
 #pragma unroll
-  for (int j = 1; j < 2 * J; ++j) ms = fmax_fx(ms, M[j]);
+  for (int j = 1; j < 2 * J; ++j) hmax = max(hmax, (int)(M[j] >> 32));
 #pragma unroll
-  for (int o = 1; o < G; o <<= 1) ms = fmax_fx(ms, __shfl_xor_sync(0xffffffffu, ms, o));
+  for (int o = 1; o < G; o <<= 1) hmax = max(hmax, __shfl_xor_sync(0xffffffffu, hmax, o));
   float tot = 0.0f;
 #pragma unroll
   for (int j = 0; j < 2 * J; ++j) {
-    term[j] = S[j] * fast_exp2(fx_diff_log2_fast(M[j] - ms));
+    const int dh = (int)(M[j] >> 32) - hmax;
+    const unsigned lo = (unsigned)((unsigned long long)M[j] & 0xffffffffull);
+    const float x2 = fmaf(__uint2float_rn(lo), kFxToLog2, (float)dh * kLog2e);
+    term[j] = S[j] * fast_exp2(x2);
     tot += term[j];
   }
 #pragma unroll
   for (int o = 1; o < G; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  *ms_out = ms;
+  *ref_out = (fx_t)hmax * (fx_t)4294967296LL;
   *tot_out = tot;
 }
 
-template <int ND, int G>
-__device__ void alpha_grouped(const Problem &p, const Workspace &ws, const Rings<ND> &r,
-                              long long b, int Tb, int Ub) {
-  constexpr int J = GroupArcs<ND, G>::J;
-  const int u = threadIdx.x / G, k = threadIdx.x % G;
-  // node index for ring reads: threads past the last row (u >= U+1, in the
-  // last warp) only join the barriers, and read row U1p - 1 so every read
-  // stays in bounds
-  const int uc = u < r.U1p ? u : r.U1p - 1;
-  const int U1 = (int)p.U1;
-  const fx_t *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * (2 * ND);
+__device__ __forceinline__ LV lv_from_sum(float tot, fx_t ms) {
+  if (!(tot > 0.0f)) return make_lv(kFxVeryNeg, 0.0f);
+  fx_t m;
+  float sv;
+  lv_normalize(tot, ms, &m, &sv);
+  return make_lv(m, sv);
+}
+
+// Per-CTA state shared by the two directions.
+struct Band {
+  int k, K;       // this CTA's band and the cluster size
+  int Rc, u_lo;   // rows [u_lo, u_lo + Rc)
+  int row, lane;  // this thread's ring row (0 .. Rc; larger = idle) and lane
+  bool control;       // the thread of the control warp that waits and releases
+  bool control_warp;  // a thread of that warp (no compute, no copies)
+  int Tb, Ub, U1;
+  int *abort;     // shared flag, set after the loop: a bounded wait gave up
+};
+
+// Halo protocol, per ring slot (a slot is reused every RA steps):
+//   full[slot]   the neighbour's value of step j has landed: armed by this
+//                CTA's control thread (arrive + expect 16 bytes), completed
+//                by the neighbour's st.async (16 bytes)
+//   empty[slot]  the neighbour has consumed step j: its control thread
+//                arrives after the barrier that ends its last read of j
+// Step j's halo value is read at steps j+1 .. j+1+max_dur, so it is released
+// at step j+2+max_dur; the producer of step j waits for the release of step
+// j - RA before storing.  The control warp issues no copies, no global
+// stores and no compute.
+
+template <int ND, int G, bool MULTI>
+__device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace &ws,
+                                              const ClusterRings<2 * ND> r, const ClusterPlan cp,
+                                              const Band bd, long long b) {
+  constexpr int REC = 2 * ND;
+  constexpr int J = (ND + G - 1) / G;
+  const int row = bd.row, k = bd.lane;
+  const int rowc = row <= cp.Rc ? row : cp.Rc;  // idle threads read in bounds
+  const int rl = rowc >= 1 ? rowc - 1 : 0;
+  const int u = bd.u_lo + row - 1;
+  const bool own = row >= 1 && row <= cp.Rc;
+  const bool lower = MULTI && bd.k > 0, upper = MULTI && bd.k + 1 < bd.K;
+  const fx_t *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * REC;
   LV *galpha = ws.alpha + b * p.n_diag * p.U1;
   int di[J], dd[J];
 #pragma unroll
@@ -367,67 +529,84 @@ __device__ void alpha_grouped(const Problem &p, const Workspace &ws, const Rings
     di[j] = k + G * j;
     dd[j] = di[j] < ND ? p.dur[di[j]] : -1;
   }
-  const int nsteps = Tb + Ub;
-  for (int q = 0; q < kPrefetch; ++q) prefetch_group<ND, G>(gdiag0, r, q, u, k, Tb, Ub, U1);
+  const int nsteps = bd.Tb + bd.Ub;
+  constexpr int P = kPrefetch;
+  const bool pref = row <= cp.Rc && !(MULTI && bd.control_warp);
+  const bool producer = upper && row == cp.Rc && k == 0;  // feeds the upper band
+  int failed = 0;  // a bounded wait of this thread gave up
+  for (int q = 0; q < P; ++q)
+    prefetch_rec<REC, G>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
   for (int s = 0; s < nsteps; ++s) {
-    prefetch_group<ND, G>(gdiag0, r, s + kPrefetch, u, k, Tb, Ub, U1);
-    cp_async_wait<kPrefetch>();
-    __syncthreads();
+    prefetch_rec<REC, G>(gdiag0, r, s + P, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
+    cp_async_wait<P>();
+    if (MULTI && bd.control && lower && s >= 1) {
+      // the lower band's value of diagonal s - 1
+      unsigned long long *f = r.full((s - 1) & r.mA);
+      arrive_expect_tx(f, (unsigned)sizeof(LV));
+      if (!wait_parity_bounded(f, ((s - 1) / r.RA) & 1)) failed = 1;
+    }
+    if (!MULTI) __syncthreads();
+    else if (__syncthreads_or(failed)) break;
+    // every thread is past step s - 1: release diagonal s - 2 - max_dur
+    if (MULTI && bd.control && lower && s - 2 - p.max_dur >= 0)
+      arrive_cluster_relaxed(map_cta(r.empty((s - 2 - p.max_dur) & r.mA), bd.k - 1));
+    if (MULTI && bd.control_warp) continue;
     const int t = s - u;
-    const bool node = u <= Ub && t >= 0 && t < Tb;
+    const bool node = own && u <= bd.Ub && t >= 0 && t < bd.Tb;
     fx_t M[2 * J];
     float S[2 * J], term[2 * J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
       const int d = dd[j];
+      const int i = di[j] < ND ? di[j] : 0;
       // blank arc (t-d, u) -> (t, u), d > 0
       const bool okb = node && d > 0 && t - d >= 0;
-      const LV ab = r.a(s - d, uc);
-      const fx_t wb = r.w(s - d, uc)[di[j] < ND ? di[j] : 0];
-      M[2 * j] = okb ? ab.m + wb : kFxVeryNeg;
+      const LV ab = r.a(s - d, rowc);
+      M[2 * j] = okb ? ab.m + r.w(s - d, rowc)[i] : kFxVeryNeg;
       S[2 * j] = okb ? ab.s : 0.0f;
       // label arc (t-d, u-1) -> (t, u), every d
       const bool okl = node && d >= 0 && u >= 1 && t - d >= 0;
-      const int ul = uc >= 1 ? uc - 1 : 0;
-      const LV al = r.a(s - d - 1, ul);
-      const fx_t wl = r.w(s - d - 1, ul)[di[j] < ND ? ND + di[j] : 0];
-      M[2 * j + 1] = okl ? al.m + wl : kFxVeryNeg;
+      const LV al = r.a(s - d - 1, rl);
+      M[2 * j + 1] = okl ? al.m + r.w(s - d - 1, rl)[ND + i] : kFxVeryNeg;
       S[2 * j + 1] = okl ? al.s : 0.0f;
     }
     fx_t ms;
     float tot;
     group_lse<J, G>(M, S, &ms, &tot, term);
-    if (node && k == 0) {
-      LV v;
-      if (s == 0) {
-        v = make_lv(0, 1.0f);
-      } else if (tot > 0.0f) {
-        fx_t m;
-        float sv;
-        lv_normalize(tot, ms, &m, &sv);
-        v = make_lv(m, sv);
-      } else {
-        v = make_lv(kFxVeryNeg, 0.0f);
-      }
-      r.a(s, u) = v;
-      galpha[(long long)s * U1 + u] = v;
+    // every lane of the group holds the node's value; lane 0 stores it
+    const LV v = node ? (s == 0 ? make_lv(0, 1.0f) : lv_from_sum(tot, ms))
+                      : make_lv(kFxVeryNeg, 0.0f);
+    if (own && k == 0) r.a(s, row) = v;
+    if (node && k == 0) galpha[(long long)s * bd.U1 + u] = v;
+    if (producer) {
+      // publish this diagonal's top row into the upper band's halo slot once
+      // that band has released the slot's previous diagonal
+      if (s >= r.RA && !wait_parity_bounded(r.empty(s & r.mA), ((s / r.RA) - 1) & 1))
+        failed = 1;
+      else
+        st_async_lv(map_cta(&r.a(s, 0), bd.k + 1), v, map_cta(r.full(s & r.mA), bd.k + 1));
     }
   }
   cp_async_wait<0>();
-  __syncthreads();
+  if (MULTI) {
+    if (__syncthreads_or(failed) && threadIdx.x == 0) *bd.abort = 1;
+  } else {
+    __syncthreads();
+  }
 }
 
-template <int ND, int G>
-__device__ void beta_grouped(const Problem &p, const Workspace &ws, const Rings<ND> &r,
-                             long long b, int Tb, int Ub) {
-  constexpr int J = GroupArcs<ND, G>::J;
-  const int u = threadIdx.x / G, k = threadIdx.x % G;
-  // node index for ring reads: threads past the last row (u >= U+1, in the
-  // last warp) only join the barriers, and read row U1p - 1 so every read
-  // stays in bounds
-  const int uc = u < r.U1p ? u : r.U1p - 1;
-  const int U1 = (int)p.U1;
-  const fx_t *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * (2 * ND);
+template <int ND, int G, bool MULTI>
+__device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &ws,
+                                             const ClusterRings<2 * ND> r, const ClusterPlan cp,
+                                             const Band bd, long long b) {
+  constexpr int REC = 2 * ND;
+  constexpr int J = (ND + G - 1) / G;
+  const int row = bd.row, k = bd.lane;
+  const int rowc = row <= cp.Rc ? row : cp.Rc;
+  const int u = bd.u_lo + row - 1;
+  const bool own = row >= 1 && row <= cp.Rc;
+  const bool lower = MULTI && bd.k > 0, upper = MULTI && bd.k + 1 < bd.K;
+  const fx_t *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * REC;
   LV *gbeta = ws.beta + b * p.n_diag * p.U1;
   const long long nodes = p.B * p.T * p.U1;
   int di[J], dd[J];
@@ -436,31 +615,49 @@ __device__ void beta_grouped(const Problem &p, const Workspace &ws, const Rings<
     di[j] = k + G * j;
     dd[j] = di[j] < ND ? p.dur[di[j]] : -1;
   }
-  const int last = Tb + Ub - 1;
-  for (int i = 0; i < kPrefetch; ++i) prefetch_group<ND, G>(gdiag0, r, last - i, u, k, Tb, Ub, U1);
-  for (int q = last; q >= 0; --q) {
-    prefetch_group<ND, G>(gdiag0, r, q - kPrefetch, u, k, Tb, Ub, U1);
-    cp_async_wait<kPrefetch>();
-    __syncthreads();
+  const int nsteps = bd.Tb + bd.Ub;
+  const int last = nsteps - 1;
+  constexpr int P = kPrefetch;
+  const bool pref = own && !(MULTI && bd.control_warp);
+  const bool producer = lower && row == 1 && k == 0;  // feeds the lower band
+  int failed = 0;  // a bounded wait of this thread gave up
+  for (int i = 0; i < P; ++i)
+    prefetch_rec<REC, G>(gdiag0, r, last - i, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
+  for (int i = 0; i < nsteps; ++i) {
+    const int q = last - i;
+    prefetch_rec<REC, G>(gdiag0, r, q - P, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
+    cp_async_wait<P>();
+    if (MULTI && bd.control && upper && i >= 1) {
+      // the upper band's value of step i - 1 (diagonal q + 1)
+      unsigned long long *f = r.full((i - 1) & r.mA);
+      arrive_expect_tx(f, (unsigned)sizeof(LV));
+      if (!wait_parity_bounded(f, ((i - 1) / r.RA) & 1)) failed = 1;
+    }
+    if (!MULTI) __syncthreads();
+    else if (__syncthreads_or(failed)) break;
+    // every thread is past step i - 1: release step i - 2 - max_dur
+    if (MULTI && bd.control && upper && i - 2 - p.max_dur >= 0)
+      arrive_cluster_relaxed(map_cta(r.empty((i - 2 - p.max_dur) & r.mA), bd.k + 1));
+    if (MULTI && bd.control_warp) continue;
     const int t = q - u;
-    const bool node = u <= Ub && t >= 0 && t < Tb;
-    const fx_t *rec = r.w(q, uc);
+    const bool node = own && u <= bd.Ub && t >= 0 && t < bd.Tb;
+    const fx_t *rec = r.w(q, rowc);
     fx_t M[2 * J];
     float S[2 * J], term[2 * J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
       const int d = dd[j];
-      const int i = di[j] < ND ? di[j] : 0;
+      const int di_ = di[j] < ND ? di[j] : 0;
       // blank arc (t, u) -> (t+d, u), d > 0; the final blank lands on T_b
-      const bool inb = node && d > 0 && t + d < Tb;
-      const bool fin = node && d > 0 && t + d == Tb && u == Ub;
-      const LV bb = r.a(q + d, uc);
-      M[2 * j] = inb ? bb.m + rec[i] : (fin ? rec[i] : kFxVeryNeg);
+      const bool inb = node && d > 0 && t + d < bd.Tb;
+      const bool fin = node && d > 0 && t + d == bd.Tb && u == bd.Ub;
+      const LV bb = r.a(q + d, rowc);
+      M[2 * j] = inb ? bb.m + rec[di_] : (fin ? rec[di_] : kFxVeryNeg);
       S[2 * j] = inb ? bb.s : (fin ? 1.0f : 0.0f);
       // label arc (t, u) -> (t+d, u+1)
-      const bool okl = node && d >= 0 && u < Ub && t + d < Tb;
-      const LV bl = r.a(q + d + 1, uc + 1 < r.U1p ? uc + 1 : uc);
-      M[2 * j + 1] = okl ? bl.m + rec[ND + i] : kFxVeryNeg;
+      const bool okl = node && d >= 0 && u < bd.Ub && t + d < bd.Tb;
+      const LV bl = r.a(q + d + 1, rowc + 1);
+      M[2 * j + 1] = okl ? bl.m + rec[ND + di_] : kFxVeryNeg;
       S[2 * j + 1] = okl ? bl.s : 0.0f;
     }
     fx_t ms;
@@ -481,49 +678,90 @@ __device__ void beta_grouped(const Problem &p, const Workspace &ws, const Rings<
       fb += __shfl_xor_sync(0xffffffffu, fb, o);
       fl += __shfl_xor_sync(0xffffffffu, fl, o);
     }
+    const LV v = node ? lv_from_sum(tot, ms) : make_lv(kFxVeryNeg, 0.0f);
+    if (own && k == 0) r.a(q, row) = v;
     if (node && k == 0) {
       ws.frac[n] = fb * inv;
       ws.frac[nodes + n] = fl * inv;
-      LV v;
-      if (tot > 0.0f) {
-        fx_t m;
-        float sv;
-        lv_normalize(tot, ms, &m, &sv);
-        v = make_lv(m, sv);
-      } else {
-        v = make_lv(kFxVeryNeg, 0.0f);
-      }
-      r.a(q, u) = v;
-      gbeta[(long long)q * U1 + u] = v;
+      gbeta[(long long)q * bd.U1 + u] = v;
+    }
+    if (producer) {
+      // publish this diagonal's bottom row into the lower band's halo slot
+      if (i >= r.RA && !wait_parity_bounded(r.empty(i & r.mA), ((i / r.RA) - 1) & 1))
+        failed = 1;
+      else
+        st_async_lv(map_cta(&r.a(q, cp.Rc + 1), bd.k - 1), v,
+                    map_cta(r.full(i & r.mA), bd.k - 1));
     }
   }
   cp_async_wait<0>();
-  __syncthreads();
+  if (MULTI) {
+    if (__syncthreads_or(failed) && threadIdx.x == 0) *bd.abort = 1;
+  } else {
+    __syncthreads();
+  }
 }
 
-template <int ND, int G>
+// Block: (Rc + 1) * G compute threads (rounded up to whole warps), then one
+// control warp when there are neighbouring bands.
+template <int ND, int G, bool MULTI>
 __global__ void __launch_bounds__(kLatticeMaxThreads, 1)
-lattice_smem_kernel(Problem p, Workspace ws, long long b0, int RA, int RW) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  const long long b = b0 + blockIdx.x;
-  const bool is_beta = blockIdx.y == 1;
+lattice_cluster_kernel(Problem p, Workspace ws, long long b0, ClusterPlan cp) {
+  constexpr int REC = 2 * ND;
+  __shared__ int s_abort;
+  const long long b = b0 + blockIdx.y;
+  const bool is_beta = blockIdx.z == 1;
+  const int kc = (int)cluster_rank();
   double sum_u;
+  // every CTA of the cluster sees the same utterance, so all return together
   const bool ok = check_utterance(p, b, &sum_u);
-  if (!is_beta && threadIdx.x == 0) write_utterance_info(p, ws, b, ok, sum_u);
+  if (!is_beta && kc == 0 && threadIdx.x == 0) write_utterance_info(p, ws, b, ok, sum_u);
   if (!ok) return;
-  Rings<ND> r;
-  r.U1p = (int)p.U1;
-  r.mA = RA - 1;
-  r.mW = RW - 1;
-  r.A = reinterpret_cast<LV *>(smem_raw);
-  r.W = reinterpret_cast<fx_t *>(r.A + RA * r.U1p);
-  const int Tb = (int)p.logit_lens[b], Ub = (int)p.label_lens[b];
-  if (!is_beta) {
-    alpha_grouped<ND, G>(p, ws, r, b, Tb, Ub);
-    if (threadIdx.x == 0) termination(p, ws, b, Tb, Ub);
-  } else {
-    beta_grouped<ND, G>(p, ws, r, b, Tb, Ub);
+  ClusterRings<REC> r;
+  r.RA = cp.RA;
+  r.mA = cp.RA - 1;
+  r.mW = cp.RW - 1;
+  r.slotA = (cp.Rc + 2) * (int)sizeof(LV);
+  r.slotW = (cp.Rc + 1) * REC * 8;
+  r.offW = (unsigned)(cp.RA * r.slotA);
+  r.offBar = r.offW + (unsigned)(cp.RW * r.slotW);
+  const int compute_threads = cp.threads - (cp.K > 1 ? 32 : 0);
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    if (MULTI) {
+      for (int i = 0; i < cp.RA; ++i) {
+        mbar_init(r.full(i), 1);
+        mbar_init(r.empty(i), 1);
+      }
+      fence_mbar_init_cluster();
+    }
   }
+  // every band's barriers exist before any band signals a neighbour
+  if (MULTI) cluster_sync_all();
+  else __syncthreads();
+  Band bd;
+  bd.k = kc;
+  bd.K = cp.K;
+  bd.Rc = cp.Rc;
+  bd.u_lo = kc * cp.Rc;
+  const bool in_compute = (int)threadIdx.x < compute_threads;
+  bd.row = in_compute ? (int)threadIdx.x / G : cp.Rc + 1;  // control warp: idle row
+  bd.lane = in_compute ? (int)threadIdx.x % G : 0;
+  bd.control = (int)threadIdx.x == compute_threads;
+  bd.control_warp = !in_compute;
+  bd.Tb = (int)p.logit_lens[b];
+  bd.Ub = (int)p.label_lens[b];
+  bd.U1 = (int)p.U1;
+  bd.abort = &s_abort;
+  if (!is_beta) alpha_cluster<ND, G, MULTI>(p, ws, r, cp, bd, b);
+  else beta_cluster<ND, G, MULTI>(p, ws, r, cp, bd, b);
+  __syncthreads();
+  if (MULTI && s_abort && threadIdx.x == 0) ws.usable[b] = 0;  // a wait timed out: NaN loss
+  // no band leaves while a neighbour may still write into its shared memory
+  if (MULTI) cluster_sync_all();
+  if (!is_beta && threadIdx.x == 0 && !s_abort && bd.Ub >= bd.u_lo &&
+      bd.Ub < bd.u_lo + cp.Rc)
+    termination(p, ws, b, bd.Tb, bd.Ub);
 }
 
 int lattice_threads(const Problem &p) {
@@ -539,48 +777,124 @@ int pow2_at_least(int v) {
   return r;
 }
 
-// Shared bytes of the ring variant, or 0 when it does not apply.
-int group_width(const Problem &p) {
-  if (p.n_dur <= kGroupMax && p.U1 * kGroupMax <= kLatticeMaxThreads) return kGroupMax;
-  return 4;
+constexpr int kMaxCluster = 16;
+constexpr size_t kClusterSmemMax = 220 * 1024;
+
+// Shape of the cluster variant for this problem with K bands, or false.
+bool cluster_plan(const Problem &p, int K, ClusterPlan *cp) {
+  if (p.n_dur > 9) return false;
+  const int G = group_lanes(p.n_dur);
+  const int Rc = (int)((p.U1 + K - 1) / K);
+  const int threads = ((Rc + 1) * G + 31) / 32 * 32 + (K > 1 ? 32 : 0);
+  if (threads > kLatticeMaxThreads) return false;
+  const int rec = arc_record_len(p.n_dur);
+  // value ring: max_dur + 2 diagonals in use, the rest is how far a band may
+  // run ahead of the band it feeds
+  const int RA = pow2_at_least(p.max_dur + 10);
+  const int RW = pow2_at_least(kPrefetch + p.max_dur + 3);
+  const size_t bytes = cluster_smem_bytes(RA, RW, Rc, rec);
+  if (bytes > kClusterSmemMax) return false;
+  cp->K = K;
+  cp->Rc = Rc;
+  cp->G = G;
+  cp->RA = RA;
+  cp->RW = RW;
+  cp->threads = threads;
+  cp->smem = bytes;
+  return true;
 }
 
-// Shared bytes of the ring variant (or 0 when it does not apply); threads =
-// (U+1) * G rounded up to whole warps.
-size_t smem_plan(const Problem &p, int *RA, int *RW, int *threads) {
-  const int G = group_width(p);
-  if (p.U1 * G > kLatticeMaxThreads || p.n_dur > 9) return 0;
-  const int th = (int)(((p.U1 * G + 31) / 32) * 32);
-  const int nodes_per_slot = (int)p.U1;
-  const int ra = pow2_at_least(p.max_dur + 2);
-  const int rw = pow2_at_least(kPrefetch + p.max_dur + 3);
-  const size_t bytes =
-      ((size_t)ra * sizeof(LV) + (size_t)rw * 16 * (size_t)p.n_dur) * (size_t)nodes_per_slot;
-  if (bytes > 200 * 1024) return 0;
-  *RA = ra;
-  *RW = rw;
-  *threads = th;
-  return bytes;
+// The fewest bands that fit: a diagonal step is latency-bound, so more bands
+// do not make it shorter, while the exchange between bands costs a share of
+// every step and each band takes an SM from the streaming passes.  One band
+// holds up to 1024 / G threads' worth of rows; then the shared-memory rings
+// decide (cluster_plan).
+int preferred_bands(const Problem &p) {
+  const int forced = g_forced_bands.load();
+  if (forced > 0) return forced < kMaxCluster ? forced : kMaxCluster;
+  return 1;
 }
 
 template <int ND, int G>
-cudaError_t launch_smem_g(const Problem &p, const Workspace &ws, long long b0, dim3 grid, int th,
-                          size_t bytes, int RA, int RW, cudaStream_t stream) {
+cudaError_t launch_cluster_g(const Problem &p, const Workspace &ws, long long b0, long long nb,
+                             bool with_beta, const ClusterPlan &cp, cudaStream_t stream,
+                             bool *placed) {
+  *placed = false;
+  auto kern = cp.K == 1 ? lattice_cluster_kernel<ND, G, false> : lattice_cluster_kernel<ND, G, true>;
   // at least kLatticeSmemFloor, so no node-table or gradient block shares the SM
-  if (bytes < (size_t)kLatticeSmemFloor) bytes = kLatticeSmemFloor;
-  cudaError_t e = cudaFuncSetAttribute(lattice_smem_kernel<ND, G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  const size_t bytes = cp.smem < (size_t)kLatticeSmemFloor ? (size_t)kLatticeSmemFloor : cp.smem;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && cp.K > 8)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
-  lattice_smem_kernel<ND, G><<<grid, th, bytes, stream>>>(p, ws, b0, RA, RW);
-  return cudaGetLastError();
+  const dim3 grid((unsigned)cp.K, (unsigned)nb, with_beta ? 2u : 1u);
+  if (cp.K == 1) {
+    // one band: an ordinary launch (a CTA outside a cluster is a cluster of one)
+    *placed = true;
+    kern<<<grid, cp.threads, bytes, stream>>>(p, ws, b0, cp);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3((unsigned)cp.threads, 1, 1);
+  cfg.dynamicSmemBytes = bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cp.K;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // a cluster of K CTAs of this size must fit the GPU at all (asked once per
+  // device and shape)
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void *, int, int, size_t>, int> fits;
+  const auto key = std::make_tuple(dev, (const void *)kern, cp.K, cp.threads, bytes);
+  int clusters = -1;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    auto it = fits.find(key);
+    if (it != fits.end()) clusters = it->second;
+  }
+  if (clusters < 0) {
+    e = cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> g(mu);
+    fits[key] = clusters;
+  }
+  *placed = clusters >= 1;
+  if (!*placed) return cudaSuccess;
+  return cudaLaunchKernelEx(&cfg, kern, p, ws, b0, cp);
 }
 
 template <int ND>
-cudaError_t launch_smem(const Problem &p, const Workspace &ws, long long b0, dim3 grid, int th,
-                        size_t bytes, int RA, int RW, cudaStream_t stream) {
-  if (ND <= kGroupMax && group_width(p) == kGroupMax)
-    return launch_smem_g<ND, kGroupMax>(p, ws, b0, grid, th, bytes, RA, RW, stream);
-  return launch_smem_g<ND, 4>(p, ws, b0, grid, th, bytes, RA, RW, stream);
+cudaError_t launch_cluster(const Problem &p, const Workspace &ws, long long b0, long long nb,
+                           bool with_beta, const ClusterPlan &cp, cudaStream_t stream,
+                           bool *placed) {
+  return launch_cluster_g<ND, group_lanes(ND)>(p, ws, b0, nb, with_beta, cp, stream, placed);
+}
+
+// Launch the cluster variant; *placed is false (nothing launched) when a
+// cluster of cp.K CTAs of this size does not fit the GPU.
+cudaError_t launch_cluster_nd(const Problem &p, const Workspace &ws, long long b0, long long nb,
+                              bool with_beta, const ClusterPlan &cp, cudaStream_t stream,
+                              bool *placed) {
+  switch (p.n_dur) {
+    case 1: return launch_cluster<1>(p, ws, b0, nb, with_beta, cp, stream, placed);
+    case 2: return launch_cluster<2>(p, ws, b0, nb, with_beta, cp, stream, placed);
+    case 3: return launch_cluster<3>(p, ws, b0, nb, with_beta, cp, stream, placed);
+    case 4: return launch_cluster<4>(p, ws, b0, nb, with_beta, cp, stream, placed);
+    case 5: return launch_cluster<5>(p, ws, b0, nb, with_beta, cp, stream, placed);
+    case 6: return launch_cluster<6>(p, ws, b0, nb, with_beta, cp, stream, placed);
+    case 7: return launch_cluster<7>(p, ws, b0, nb, with_beta, cp, stream, placed);
+    case 8: return launch_cluster<8>(p, ws, b0, nb, with_beta, cp, stream, placed);
+    default: return launch_cluster<9>(p, ws, b0, nb, with_beta, cp, stream, placed);
+  }
 }
 
 // ---------------------------------------------------------------- reduction
@@ -624,29 +938,35 @@ __global__ void reduce_kernel(Problem p, Workspace ws, float *loss_out) {
 
 }  // namespace
 
+
 cudaError_t launch_lattice(const Problem &p, const Workspace &ws, long long b_begin,
                            long long b_end, bool with_beta, cudaStream_t stream) {
-  const long long nb = b_end - b_begin;
-  if (nb <= 0) return cudaSuccess;
-  int RA = 0, RW = 0, th = 0;
-  const size_t bytes = smem_plan(p, &RA, &RW, &th);
-  if (bytes > 0) {
-    const dim3 grid((unsigned)nb, with_beta ? 2u : 1u);
-    switch (p.n_dur) {
-      case 1: return launch_smem<1>(p, ws, b_begin, grid, th, bytes, RA, RW, stream);
-      case 2: return launch_smem<2>(p, ws, b_begin, grid, th, bytes, RA, RW, stream);
-      case 3: return launch_smem<3>(p, ws, b_begin, grid, th, bytes, RA, RW, stream);
-      case 4: return launch_smem<4>(p, ws, b_begin, grid, th, bytes, RA, RW, stream);
-      case 5: return launch_smem<5>(p, ws, b_begin, grid, th, bytes, RA, RW, stream);
-      case 6: return launch_smem<6>(p, ws, b_begin, grid, th, bytes, RA, RW, stream);
-      case 7: return launch_smem<7>(p, ws, b_begin, grid, th, bytes, RA, RW, stream);
-      case 8: return launch_smem<8>(p, ws, b_begin, grid, th, bytes, RA, RW, stream);
-      default: return launch_smem<9>(p, ws, b_begin, grid, th, bytes, RA, RW, stream);
+  // grid.y is at most 65535: launch in groups of utterances
+  for (long long g0 = b_begin; g0 < b_end; g0 += 65535) {
+    const long long nb = (b_end - g0 < 65535) ? b_end - g0 : 65535;
+    bool done = false;
+    // K bands per utterance: the preferred count, else more bands (fewer
+    // rows, when a band needs too many threads or too much shared memory),
+    // else fewer (when a cluster of K CTAs does not fit the GPU)
+    const int K0 = preferred_bands(p);
+    for (int step = 0; step < 2 * kMaxCluster && !done; ++step) {
+      const int K = step < kMaxCluster - K0 + 1 ? K0 + step : K0 - (step - (kMaxCluster - K0));
+      if (K < 1 || K > kMaxCluster) continue;
+      ClusterPlan cp;
+      if (!cluster_plan(p, K, &cp)) continue;
+      bool placed = false;
+      const cudaError_t e = launch_cluster_nd(p, ws, g0, nb, with_beta, cp, stream, &placed);
+      if (e != cudaSuccess) return e;
+      done = placed;
+    }
+    if (!done) {
+      alpha_kernel<<<(unsigned)nb, lattice_threads(p), 0, stream>>>(p, ws, g0);
+      if (with_beta) beta_kernel<<<(unsigned)nb, lattice_threads(p), 0, stream>>>(p, ws, g0);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
     }
   }
-  alpha_kernel<<<(unsigned)nb, lattice_threads(p), 0, stream>>>(p, ws, b_begin);
-  if (with_beta) beta_kernel<<<(unsigned)nb, lattice_threads(p), 0, stream>>>(p, ws, b_begin);
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_reduce(const Problem &p, const Workspace &ws, float *loss_out,
@@ -656,3 +976,8 @@ cudaError_t launch_reduce(const Problem &p, const Workspace &ws, float *loss_out
 }
 
 }  // namespace tdt
+
+extern "C" int tdt_loss_set_lattice_bands(int bands) {
+  if (bands < 0) bands = 0;
+  return tdt::g_forced_bands.exchange(bands);
+}

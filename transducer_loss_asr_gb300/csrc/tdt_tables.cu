@@ -16,9 +16,10 @@
 //
 // Outputs per usable node (t < T_b, u <= U_b):
 //   lse_tok[n], lse_dur[n]   float, for the gradient pass
-//   arcw[g][0..2D)           fx arc log-weights lpB - sigma + lpD_i and
-//                            lpL - sigma + lpD_i, anti-diagonal layout, one
-//                            contiguous record per node for the lattice passes
+//   arcw[g][0..2D)           node arc record in fx (tdt_common.cuh): blank
+//                            and label arc log-weights per duration,
+//                            anti-diagonal layout, one contiguous record per
+//                            node for the lattice passes
 #include "tdt_rowio.cuh"
 
 namespace tdt {
@@ -156,8 +157,8 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
   const fx_t lse_fx = fx_from_float(M) + fx_log_ge1(S);
   const fx_t lsed_fx = fx_from_float(md) + fx_log_ge1(sd);
 
-  // arc log-weights of this node: [i] blank arc with duration i, [D + i]
-  // label arc with duration i
+  // the node's arc record: [i] blank arc with duration i, [D + i] label arc
+  // with duration i (token log-prob - sigma + duration log-prob)
   const float zb = Elem<DT>::load(row + p.blank);
   const fx_t wbs = clamp_lp(fx_from_float(zb) - lse_fx) - p.sigma_fx;
   fx_t wls = 0;
@@ -166,7 +167,7 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
     if (y >= 0 && y < p.V && y != p.blank)
       wls = clamp_lp(fx_from_float(Elem<DT>::load(row + y)) - lse_fx) - p.sigma_fx;
   }
-  fx_t *rec = ws.arcw + diag_index(p, b, t, u) * (2 * p.D);
+  fx_t *rec = ws.arcw + diag_index(p, b, t, u) * p.rec_len;
   for (int i = lt; i < p.D; i += TPR) {
     const fx_t ld = clamp_lp(fx_from_float(Elem<DT>::load(row + p.V + i)) - lsed_fx);
     rec[i] = wbs + ld;
