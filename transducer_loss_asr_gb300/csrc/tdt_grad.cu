@@ -43,12 +43,13 @@ __device__ __forceinline__ void zero_row(typename Elem<DT>::T *out, long long VD
 }
 
 template <int DT, int TPR, bool COH>
-__global__ void __launch_bounds__(kGradThreads)
+__global__ void __launch_bounds__(kGradThreads, TPR == 256 ? 4 : 3)
 grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gscale,
             long long n_begin, long long n_end) {
   typedef typename Elem<DT>::T E;
   constexpr int N = Vec<DT>::N;
   constexpr int RPB = kGradThreads / TPR;
+  constexpr int kDurPerLane = (kMaxDurations + TPR - 1) / TPR;  // D <= kMaxDurations
   const E *logits = static_cast<const E *>(p.logits);
   const int lt = threadIdx.x % TPR;
   const long long n = n_begin + (long long)blockIdx.x * RPB + threadIdx.x / TPR;
@@ -59,31 +60,46 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
   const long long Tb = p.logit_lens[b], Ub = p.label_lens[b];
   const E *row = logits + b * p.s0 + t * p.s1 + u * p.s2;
   const bool in_lattice = t < Tb && u <= Ub;
-  // Row geometry, and the first batch of 16-byte loads issued before the
-  // per-row coefficients are fetched, so the two latencies overlap.
+  // Everything the row needs is loaded up front, so its latencies overlap:
+  // the first batch of 16-byte vectors, the scalar head and tail, the
+  // duration logits and their coefficients (lane lt: durations lt, lt + TPR,
+  // ...), the row's coefficient record and the upstream gradient.
   const uintptr_t ai = reinterpret_cast<uintptr_t>(row), ao = reinterpret_cast<uintptr_t>(out);
   const bool vec = ((ai ^ ao) & 15) == 0;
   int head = head_elems<DT>(row);
   if (head > p.V) head = (int)p.V;
   const int nvec = (int)((p.V - head) / N);
+  const long long tail0 = head + (long long)nvec * N;
+  const int ntail = (int)(p.V - tail0);
   const uint4 *vin = reinterpret_cast<const uint4 *>(row + head);
+  const float *rc = ws.rowc + n * p.rc_stride;
   uint4 v[kBatch];
-  if (in_lattice && vec) {
+  float zh = 0.0f, zt = 0.0f, zd[kDurPerLane], rcd[kDurPerLane];
+  if (in_lattice) {
+    if (vec) {
 #pragma unroll
-    for (int i = 0; i < kBatch; ++i) {
-      const int j = i * TPR + lt;
-      if (j < nvec) v[i] = ld_row16<COH>(vin + j);
+      for (int i = 0; i < kBatch; ++i) {
+        const int j = i * TPR + lt;
+        if (j < nvec) v[i] = ld_row16<COH>(vin + j);
+      }
+      if (lt < head) zh = ld_elem<DT, COH>(row + lt);
+      if (lt < ntail) zt = ld_elem<DT, COH>(row + tail0 + lt);
+    }
+#pragma unroll
+    for (int c = 0; c < kDurPerLane; ++c) {
+      const int i = lt + c * TPR;
+      zd[c] = i < p.D ? ld_elem<DT, COH>(row + p.V + i) : 0.0f;
+      rcd[c] = i < p.D ? rc[kRcD + i] : 0.0f;
     }
   }
-  const float *rc = ws.rowc + n * p.rc_stride;
+  // upstream gradient of utterance b's loss (1 when none is given; x * 1 is exact)
+  const float gs = gscale ? gscale[p.reduction == kNone ? b : 0] : 1.0f;
   const float4 r0 = *reinterpret_cast<const float4 *>(rc);
   const float4 r1 = *reinterpret_cast<const float4 *>(rc + 4);
   if (!in_lattice || r1.z == 0.0f) {
     zero_row<DT, TPR>(out, p.VD, lt);
     return;
   }
-  // upstream gradient of utterance b's loss (1 when none is given; x * 1 is exact)
-  const float gs = gscale ? gscale[p.reduction == kNone ? b : 0] : 1.0f;
   const float a = r0.x * gs, lse2 = r0.y, lsed2 = r0.z, ab = r0.w * gs, al = r1.x * gs;
   const int y = __float_as_int(r1.y);
   auto g_at = [&](float x, long long k) {
@@ -94,13 +110,8 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
   };
 
   if (vec) {
-    const long long tail0 = head + (long long)nvec * N;
-    const int ntail = (int)(p.V - tail0);
-    if (lt < head) out[lt] = Elem<DT>::from_float(g_at(ld_elem<DT, COH>(row + lt), lt));
-    if (lt < ntail) {
-      const long long k = tail0 + lt;
-      out[k] = Elem<DT>::from_float(g_at(ld_elem<DT, COH>(row + k), k));
-    }
+    if (lt < head) out[lt] = Elem<DT>::from_float(g_at(zh, lt));
+    if (lt < ntail) out[tail0 + lt] = Elem<DT>::from_float(g_at(zt, tail0 + lt));
     uint4 *vout = reinterpret_cast<uint4 *>(out + head);
     // vectors holding the two special entries (or -1)
     const int jb = (p.blank >= head && p.blank < tail0) ? (int)((p.blank - head) / N) : -1;
@@ -143,10 +154,12 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
       }
     }
   }
-  for (int i = lt; i < p.D; i += TPR) {
-    const float zd = ld_elem<DT, COH>(row + p.V + i);
-    out[p.V + i] =
-        Elem<DT>::from_float(a * fast_exp2(fmaf(zd, kLog2e, -lsed2)) - rc[kRcD + i] * gs);
+#pragma unroll
+  for (int c = 0; c < kDurPerLane; ++c) {
+    const int i = lt + c * TPR;
+    if (i < p.D)
+      out[p.V + i] =
+          Elem<DT>::from_float(a * fast_exp2(fmaf(zd[c], kLog2e, -lsed2)) - rcd[c] * gs);
   }
 }
 

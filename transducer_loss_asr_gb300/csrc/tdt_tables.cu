@@ -30,6 +30,7 @@ constexpr int kTablesThreads = 256;
 constexpr int kBatch = 8;          // 16-byte loads issued per thread before use
 constexpr int kVecPerThread = 16;  // row vectors per thread when choosing TPR
 
+
 __device__ __forceinline__ fx_t clamp_lp(fx_t v) {
   const fx_t floor_fx = (fx_t)kLogProbFloor * (fx_t)4294967296LL;
   return v < floor_fx ? floor_fx : v;
@@ -72,11 +73,12 @@ __device__ __forceinline__ void group_ms(float &m, float &s, float *sm_m, float 
 }
 
 template <int DT, int TPR>
-__global__ void __launch_bounds__(kTablesThreads)
+__global__ void __launch_bounds__(kTablesThreads, 4)
 node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) {
   typedef typename Elem<DT>::T E;
   constexpr int N = Vec<DT>::N;
   constexpr int RPB = kTablesThreads / TPR;
+  constexpr int kDurPerLane = (kMaxDurations + TPR - 1) / TPR;  // D <= kMaxDurations
   __shared__ float sm_m[kTablesThreads / 32], sm_s[kTablesThreads / 32];
   const E *logits = static_cast<const E *>(p.logits);
   const int lt = threadIdx.x % TPR;
@@ -91,20 +93,37 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
   }
   const E *row = logits + b * p.s0 + t * p.s1 + u * p.s2;
 
+  // Everything of the row that does not depend on its reduction is loaded up
+  // front, so the row costs one memory round trip (plus one for the label's
+  // logit) rather than one per part: the duration logits (lane lt holds
+  // durations lt, lt + TPR, ...), the blank logit, the label and its logit.
+  float zd[kDurPerLane];
+  float zb = 0.0f, zy = 0.0f;
+  long long y = -1;
+  int head = 0, nvec = 0, ntail = 0;
+  float zh = 0.0f, zt = 0.0f;
+  if (active) {
+#pragma unroll
+    for (int c = 0; c < kDurPerLane; ++c) {
+      const int i = lt + c * TPR;
+      zd[c] = i < p.D ? Elem<DT>::load(row + p.V + i) : -INFINITY;
+    }
+    zb = Elem<DT>::load(row + p.blank);
+    if (u < Ub) y = p.labels[b * (p.U1 - 1) + u];
+    head = head_elems<DT>(row);
+    if (head > p.V) head = (int)p.V;
+    nvec = (int)((p.V - head) / N);
+    const int tail0 = head + nvec * N;
+    ntail = (int)(p.V - tail0);
+    // head (< N elements) and tail (< N elements) each on lanes 0.., TPR >= N
+    if (lt < head) zh = Elem<DT>::load(row + lt);
+    if (lt < ntail) zt = Elem<DT>::load(row + tail0 + lt);
+  }
+  const bool y_ok = y >= 0 && y < p.V && y != p.blank;
+
   // token logits [0, V)
   float m = -INFINITY, s = 0.0f;
   if (active) {
-    int head = head_elems<DT>(row);
-    if (head > p.V) head = (int)p.V;
-    const int nvec = (int)((p.V - head) / N);
-    const int tail0 = head + nvec * N;
-    const int ntail = (int)(p.V - tail0);
-    // head (< N elements) and tail (< N elements) each on lanes 0.., TPR >= N
-    if (lt < head) {
-      m = Elem<DT>::load(row + lt);
-      s = 1.0f;
-    }
-    if (lt < ntail) merge_ms(m, s, Elem<DT>::load(row + tail0 + lt), 1.0f);
     const uint4 *vbase = reinterpret_cast<const uint4 *>(row + head);
     for (int j0 = 0; j0 < nvec; j0 += TPR * kBatch) {
       uint4 v[kBatch];
@@ -113,6 +132,8 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
         const int j = j0 + i * TPR + lt;
         if (j < nvec) v[i] = ld_row16<false>(vbase + j);
       }
+      // the label's logit, once the label has arrived (overlaps the batch)
+      if (j0 == 0 && y_ok) zy = Elem<DT>::load(row + y);
       float cm = -INFINITY;
 #pragma unroll
       for (int i = 0; i < kBatch; ++i) {
@@ -140,17 +161,19 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
         }
       }
     }
+    if (nvec == 0 && y_ok) zy = Elem<DT>::load(row + y);
+    if (lt < head) merge_ms(m, s, zh, 1.0f);
+    if (lt < ntail) merge_ms(m, s, zt, 1.0f);
   }
   group_ms<TPR>(m, s, sm_m, sm_s);
   const float M = m, S = s;
 
-  // duration logits [V, V+D): thread lt takes durations lt, lt+TPR, ...
+  // duration logits [V, V+D)
   float md = -INFINITY, sd = 0.0f;
   if (active) {
-    for (int i = lt; i < p.D; i += TPR) {
-      const float z = Elem<DT>::load(row + p.V + i);
-      merge_ms(md, sd, z, 1.0f);
-    }
+#pragma unroll
+    for (int c = 0; c < kDurPerLane; ++c)
+      if (lt + c * TPR < p.D) merge_ms(md, sd, zd[c], 1.0f);
   }
   group_ms<TPR>(md, sd, sm_m, sm_s);
   if (!active) return;
@@ -159,19 +182,17 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
 
   // the node's arc record: [i] blank arc with duration i, [D + i] label arc
   // with duration i (token log-prob - sigma + duration log-prob)
-  const float zb = Elem<DT>::load(row + p.blank);
   const fx_t wbs = clamp_lp(fx_from_float(zb) - lse_fx) - p.sigma_fx;
-  fx_t wls = 0;
-  if (u < Ub) {
-    const long long y = p.labels[b * (p.U1 - 1) + u];
-    if (y >= 0 && y < p.V && y != p.blank)
-      wls = clamp_lp(fx_from_float(Elem<DT>::load(row + y)) - lse_fx) - p.sigma_fx;
-  }
+  const fx_t wls = y_ok ? clamp_lp(fx_from_float(zy) - lse_fx) - p.sigma_fx : 0;
   fx_t *rec = ws.arcw + diag_index(p, b, t, u) * p.rec_len;
-  for (int i = lt; i < p.D; i += TPR) {
-    const fx_t ld = clamp_lp(fx_from_float(Elem<DT>::load(row + p.V + i)) - lsed_fx);
-    rec[i] = wbs + ld;
-    rec[p.D + i] = wls + ld;
+#pragma unroll
+  for (int c = 0; c < kDurPerLane; ++c) {
+    const int i = lt + c * TPR;
+    if (i < p.D) {
+      const fx_t ld = clamp_lp(fx_from_float(zd[c]) - lsed_fx);
+      rec[i] = wbs + ld;
+      rec[p.D + i] = wls + ld;
+    }
   }
   if (lt == 0) {
     ws.lse_tok[n] = M + logf(S);
