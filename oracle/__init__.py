@@ -5,9 +5,10 @@ Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 (``transducer_loss_asr_gb300``) never imports it, and this package imports
 nothing from the product: the two share no code.
 
-The arithmetic lives in ``tdt_oracle.c`` (plain float64 C, OpenMP only over
-independent utterances and nodes); this module compiles it with gcc and
-marshals numpy arrays into it.  See the header of ``tdt_oracle.c`` for the
+The arithmetic lives in ``tdt_oracle.c`` (the TDT loss) and
+``rnnt_oracle.c`` (the plain RNN-T loss, no duration head), plain float64 C
+with OpenMP only over independent utterances and nodes; this module compiles
+them with gcc and marshals numpy arrays into them.  See the header of ``tdt_oracle.c`` for the
 passages of "tdt-loss: add TDT loss kernel" (kernels-community PR #882) and
 "Add TDT loss kernel" (transformers PR #46048) that it follows, and for the
 reading of the lattice it writes out.
@@ -28,6 +29,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "tdt_oracle.c")
+_SRCS = (_SRC, os.path.join(_HERE, "rnnt_oracle.c"))
 _LIB_PATH = os.path.join(_HERE, "libtdt_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -36,12 +38,13 @@ REDUCTIONS = {"none": 0, "sum": 1, "mean": 2, "mean_batch": 3, "mean_volume": 4}
 
 
 def build(force: bool = False) -> str:
-    """Compile tdt_oracle.c into libtdt_oracle.so next to it (gcc, -O2, OpenMP)."""
+    """Compile tdt_oracle.c and rnnt_oracle.c into libtdt_oracle.so next to
+    them (gcc, -O2, OpenMP)."""
     if (not force and os.path.exists(_LIB_PATH)
-            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB_PATH) >= os.path.getmtime(f) for f in _SRCS)):
         return _LIB_PATH
     tmp = _LIB_PATH + ".tmp.%d" % os.getpid()
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-o", tmp, _SRC, "-lm"]
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-o", tmp, *_SRCS, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -59,6 +62,11 @@ def load_library(path: str):
     lib.tdt_oracle_tables.restype = ctypes.c_int
     lib.tdt_oracle_tables.argtypes = [
         P, ctypes.c_int, P, P, P, I64, P, P, ctypes.c_int, ctypes.c_int, P, P, P, P]
+    if hasattr(lib, "rnnt_oracle_run"):  # absent from single-file test variants
+        lib.rnnt_oracle_run.restype = ctypes.c_int
+        lib.rnnt_oracle_run.argtypes = [
+            P, ctypes.c_int, P, P, P, I64, P, P, ctypes.c_int, ctypes.c_double, ctypes.c_int,
+            P, P, P, P, P, P, P, P]
     return lib
 
 
@@ -157,6 +165,42 @@ def tdt_loss(logits: np.ndarray, labels: np.ndarray, logit_lens: np.ndarray,
         _ptr(lla), _ptr(llb), _ptr(rows_arr), n_rows, _ptr(grad))
     if rc != 0:
         raise ValueError("tdt_oracle_run rejected its arguments (status %d)" % rc)
+    return OracleResult(loss, utt, scale, lla, llb, alpha, beta, grad)
+
+
+def rnnt_loss(logits: np.ndarray, labels: np.ndarray, logit_lens: np.ndarray,
+              label_lens: np.ndarray, blank: int, sigma: float = 0.0,
+              reduction: str = "mean_volume", want_grad: bool = True,
+              want_lattice: bool = False, lib=None) -> OracleResult:
+    """Plain RNN-T loss (no duration head) and its gradient in float64
+    (rnnt_oracle.c).  logits [B, T, U+1, V], any element strides; the other
+    arguments as for tdt_loss.  grad has the logits' shape."""
+    lib = _load() if lib is None else lib
+    f64, strides = _logits_view(logits)
+    B, T, U1, V = logits.shape
+    sizes = np.array([B, T, U1, V], dtype=np.int64)
+    labels = np.ascontiguousarray(labels, dtype=np.int64)
+    if labels.ndim != 2 or labels.shape[0] != B or labels.shape[1] < U1 - 1:
+        raise ValueError("labels must be [B, >= U]")
+    lstride = labels.shape[1]
+    if lstride == 0:
+        labels = np.zeros((B, 1), dtype=np.int64)
+        lstride = 1
+    logit_lens = np.ascontiguousarray(logit_lens, dtype=np.int64)
+    label_lens = np.ascontiguousarray(label_lens, dtype=np.int64)
+    red = REDUCTIONS[reduction]
+    loss = np.zeros(B if red == 0 else 1)
+    utt = np.zeros(B); scale = np.zeros(B); lla = np.zeros(B); llb = np.zeros(B)
+    alpha = np.zeros((B, T, U1)) if want_lattice else None
+    beta = np.zeros((B, T, U1)) if want_lattice else None
+    grad = np.zeros((B, T, U1, V)) if want_grad else None
+    rc = lib.rnnt_oracle_run(
+        logits.ctypes.data_as(ctypes.c_void_p), f64, _ptr(sizes), _ptr(strides), _ptr(labels),
+        lstride, _ptr(logit_lens), _ptr(label_lens), int(blank), float(sigma), red,
+        _ptr(loss), _ptr(utt), _ptr(scale), _ptr(alpha), _ptr(beta), _ptr(lla), _ptr(llb),
+        _ptr(grad))
+    if rc != 0:
+        raise ValueError("rnnt_oracle_run rejected its arguments (status %d)" % rc)
     return OracleResult(loss, utt, scale, lla, llb, alpha, beta, grad)
 
 
