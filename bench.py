@@ -158,8 +158,11 @@ def oracle_sample(inp, max_utts=1, frames=None):
     oracle.build()
 
     def run():
-        oracle.tdt_loss(z, labels, tl, ul, inp["durations"], inp["blank"], inp["sigma"],
-                        inp["reduction"])
+        if w.loss == "rnnt":
+            oracle.rnnt_loss(z, labels, tl, ul, inp["blank"], inp["sigma"], inp["reduction"])
+        else:
+            oracle.tdt_loss(z, labels, tl, ul, inp["durations"], inp["blank"], inp["sigma"],
+                            inp["reduction"])
 
     return run, sample_bytes, "%d of %d utterances, %d of %d frames (%d lattice rows of %d)" % (
         b, w.B, T, w.T, valid, w.B * w.T * (w.U + 1))
@@ -214,7 +217,7 @@ def config_dict(w, l2):
         " view of width %d" % w.base_vd if w.base_vd else "", w.sigma, w.reduction),
         "lengths": "full" if w.T_range is None else "T_b in %s, U_b in %s" % (w.T_range,
                                                                              w.U_range),
-        "l2": l2, "global_batch": w.B}
+        "l2": l2, "global_batch": w.B, "loss": w.loss}
 
 
 def main():
@@ -272,10 +275,17 @@ def main():
     loss = torch.empty(w.B if w.reduction == "none" else 1, dtype=torch.float32, device=dev)
     grad = torch.empty(logits.shape, dtype=logits.dtype, device=dev)
 
+    def call(z, labels, tl, ul):
+        if w.loss == "rnnt":
+            binding.tdt_rnnt_loss_fwd_bwd(z, labels, tl, ul, inp["blank"], inp["sigma"],
+                                          inp["reduction"], loss_out=loss, grad_out=grad)
+        else:
+            binding.tdt_loss_fwd_bwd(z, labels, tl, ul, inp["durations"], inp["blank"],
+                                     inp["sigma"], inp["reduction"], loss_out=loss,
+                                     grad_out=grad)
+
     def step():
-        binding.tdt_loss_fwd_bwd(logits, inp["labels"], inp["logit_lens"], inp["label_lens"],
-                                 inp["durations"], inp["blank"], inp["sigma"], inp["reduction"],
-                                 loss_out=loss, grad_out=grad)
+        call(logits, inp["labels"], inp["logit_lens"], inp["label_lens"])
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -336,8 +346,7 @@ def main():
         labels_d.copy_(labels_h, non_blocking=True)
         tl_d.copy_(tl_h, non_blocking=True)
         ul_d.copy_(ul_h, non_blocking=True)
-        binding.tdt_loss_fwd_bwd(view_d, labels_d, tl_d, ul_d, inp["durations"], inp["blank"],
-                                 inp["sigma"], inp["reduction"], loss_out=loss, grad_out=grad)
+        call(view_d, labels_d, tl_d, ul_d)
         loss_h.copy_(loss, non_blocking=True)
         grad_h.copy_(grad, non_blocking=True)
 

@@ -115,6 +115,22 @@ int tdt_loss_fwd_bwd(const void *logits, const int64_t sizes[4], const int64_t s
                      double sigma, int reduction, float *loss_out, void *grad_out, void *stream);
 
 /*
+ * Plain RNN-T loss (no duration head) and its gradient, on the same kernels:
+ * "Add TDT loss kernel" (transformers PR #46048), commit list, notes that
+ * torchaudio's rnnt_loss does not train the duration head -- this is that
+ * loss.  Lattice: blank arc (t,u)->(t+1,u), label arc (t,u)->(t,u+1), a path
+ * ends with the blank arc from (T_b-1, U_b); arc weight = token log-prob -
+ * sigma (sigma = 0: the textbook loss).
+ *   logits  [B, T, U+1, V] (no duration logits), sizes = {B, T, U+1, V};
+ *   every other argument as for tdt_loss_fwd_bwd (no durations);
+ *   grad_out contiguous [B, T, U+1, V] or NULL; may be the logits (in place).
+ */
+int tdt_rnnt_loss_fwd_bwd(const void *logits, const int64_t sizes[4], const int64_t strides[4],
+                          int dtype, const int64_t *labels, const int64_t *logit_lens,
+                          const int64_t *label_lens, int blank, double sigma, int reduction,
+                          float *loss_out, void *grad_out, void *stream);
+
+/*
  * Bytes of device scratch that tdt_loss_fwd_bwd_ws needs for these sizes
  * (0 for invalid arguments).  The value depends only on sizes and n_dur.
  */

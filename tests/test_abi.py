@@ -202,3 +202,22 @@ def test_autograd_op_fake_shapes_and_cpu_rejection(lib):
     with pytest.raises(NotImplementedError):
         autograd.tdt_loss(torch.zeros(2, 5, 3, 13), torch.zeros(2, 2, dtype=torch.long),
                           torch.full((2,), 5), torch.full((2,), 2), [0, 1, 2], 6)
+
+
+def test_rnnt_entry_validates(lib):
+    so = lib.lib
+    f = ctypes.c_void_p(FAKE)
+
+    def call(sizes, strides, dtype=0, blank=6, red=4, grad=f, sigma=0.0):
+        return so.tdt_rnnt_loss_fwd_bwd(f, (ctypes.c_int64 * 4)(*sizes),
+                                        (ctypes.c_int64 * 4)(*strides), dtype, f, f, f, blank,
+                                        sigma, red, f, grad, None)
+
+    ok_sizes, ok_strides = [2, 5, 3, 10], [150, 30, 10, 1]
+    assert call([2, 5, 3, 0], ok_strides) == -2          # V >= 1
+    assert call(ok_sizes, ok_strides, blank=10) == -6      # blank < V = 10 (no duration logits)
+    assert call(ok_sizes, ok_strides, dtype=5) == -4
+    assert call(ok_sizes, ok_strides, red=9) == -7
+    assert call(ok_sizes, ok_strides, sigma=float("inf")) == -8
+    assert call(ok_sizes, [150, 30, 10, 2]) == -3
+    assert call(ok_sizes, ok_strides, grad=ctypes.c_void_p(FAKE + 4)) == -13

@@ -44,6 +44,8 @@ def _load() -> ctypes.CDLL:
     lib.tdt_loss_fwd_bwd_ws.argtypes = common + [P, ctypes.c_size_t, P]
     lib.tdt_loss_fwd_bwd_noalloc.restype = I
     lib.tdt_loss_fwd_bwd_noalloc.argtypes = common + [P]
+    lib.tdt_rnnt_loss_fwd_bwd.restype = I
+    lib.tdt_rnnt_loss_fwd_bwd.argtypes = [P, P, P, I, P, P, P, I, ctypes.c_double, I, P, P, P]
     lib.tdt_loss_fwd.restype = I
     lib.tdt_loss_fwd.argtypes = common[:-1] + [P, ctypes.c_size_t, P]
     lib.tdt_loss_bwd.restype = I
@@ -132,6 +134,21 @@ def tdt_loss_fwd_bwd(logits, labels, logit_lens, label_lens, durations, blank, s
                                         compute_grad)
     with torch.cuda.device(logits.device):
         _check(lib.tdt_loss_fwd_bwd(*args, _stream_handle(logits.device)))
+    return loss_out, grad_out
+
+
+def tdt_rnnt_loss_fwd_bwd(logits, labels, logit_lens, label_lens, blank, sigma=0.0,
+                          reduction="mean_volume", loss_out=None, grad_out=None,
+                          compute_grad=True):
+    """Plain RNN-T loss (no duration head) and its gradient on the current
+    CUDA stream: logits [B, T, U+1, V]; other arguments as tdt_loss_fwd_bwd
+    without durations.  Returns (loss, grad)."""
+    args, loss_out, grad_out = _marshal(logits, labels, logit_lens, label_lens, [0], blank,
+                                        sigma, reduction, loss_out, grad_out, compute_grad)
+    # drop the durations pointer and count of the TDT argument list
+    rargs = args[:7] + args[9:]
+    with torch.cuda.device(logits.device):
+        _check(lib.tdt_rnnt_loss_fwd_bwd(*rargs, _stream_handle(logits.device)))
     return loss_out, grad_out
 
 

@@ -76,7 +76,15 @@ size_t elem_size(int dtype) { return dtype == TDT_DTYPE_F32 ? 4 : 2; }
 int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4], int dtype,
              const int64_t *labels, const int64_t *logit_lens, const int64_t *label_lens,
              const int32_t *durations, int n_dur, int blank, double sigma, int reduction,
-             const float *loss_out, const void *grad_out, Problem *p, bool need_loss) {
+             const float *loss_out, const void *grad_out, Problem *p, bool need_loss,
+             bool rnnt) {
+  // plain RNN-T: no duration logits; the lattice has durations {0, 1}
+  static const int32_t kRnntDurations[2] = {0, 1};
+  if (rnnt) {
+    durations = kRnntDurations;
+    n_dur = 2;
+  }
+  const int n_dur_logits = rnnt ? 0 : n_dur;
   if (!sizes || !strides || !durations) return TDT_ERR_NULL_POINTER;
   // loss_out may be NULL only when it has no elements (empty batch, reduction none)
   if (need_loss && !loss_out && !(sizes[0] == 0 && reduction == TDT_REDUCTION_NONE))
@@ -85,7 +93,7 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
     return TDT_ERR_BAD_DTYPE;
   if (n_dur < 1 || n_dur > kMaxDurations) return TDT_ERR_BAD_DURATIONS;
   const long long B = sizes[0], T = sizes[1], U1 = sizes[2], VD = sizes[3];
-  if (B < 0 || T < 1 || U1 < 1 || VD <= n_dur) return TDT_ERR_BAD_SIZES;
+  if (B < 0 || T < 1 || U1 < 1 || VD <= n_dur_logits) return TDT_ERR_BAD_SIZES;
   if (T + U1 > 65536) return TDT_ERR_BAD_SIZES;
   if (B * T * U1 >= (1LL << 31)) return TDT_ERR_BAD_SIZES;
   if (B > 0 && (!logits || !logit_lens || !label_lens)) return TDT_ERR_NULL_POINTER;
@@ -99,7 +107,7 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
       if (durations[j] == durations[i]) return TDT_ERR_BAD_DURATIONS;
     if (durations[i] > max_dur) max_dur = durations[i];
   }
-  const long long V = VD - n_dur;
+  const long long V = VD - n_dur_logits;
   if (blank < 0 || blank >= V) return TDT_ERR_BAD_BLANK;
   if (reduction < TDT_REDUCTION_NONE || reduction > TDT_REDUCTION_MEAN_VOLUME)
     return TDT_ERR_BAD_REDUCTION;
@@ -122,7 +130,7 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
 
   memset(p, 0, sizeof(*p));
   p->logits = logits;
-  p->B = B; p->T = T; p->U1 = U1; p->VD = VD; p->V = V; p->D = n_dur;
+  p->B = B; p->T = T; p->U1 = U1; p->VD = VD; p->V = V; p->D = n_dur_logits;
   p->s0 = strides[0]; p->s1 = strides[1]; p->s2 = strides[2];
   p->labels = reinterpret_cast<const long long *>(labels);
   p->logit_lens = reinterpret_cast<const long long *>(logit_lens);
@@ -136,6 +144,7 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
   p->n_diag = T + U1 - 1;
   p->rc_stride = row_coeff_stride(n_dur);
   p->rec_len = arc_record_len(n_dur);
+  p->rnnt = rnnt ? 1 : 0;
   return TDT_OK;
 }
 
@@ -373,6 +382,25 @@ int tdt_loss_fwd_bwd(const void *logits, const int64_t sizes[4], const int64_t s
   if (rc != TDT_OK) return rc;
   tdt::Layout L;
   if (!tdt::make_layout(sizes, n_dur, &L)) return TDT_ERR_BAD_SIZES;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  void *ws_ptr = nullptr;
+  if (cudaMallocAsync(&ws_ptr, L.total, s) != cudaSuccess) return TDT_ERR_CUDA;
+  tdt::Workspace ws = tdt::carve(L, ws_ptr);
+  rc = tdt::run(p, dtype, ws, loss_out, grad_out, nullptr, false, s);
+  if (cudaFreeAsync(ws_ptr, s) != cudaSuccess && rc == TDT_OK) rc = TDT_ERR_CUDA;
+  return rc;
+}
+
+int tdt_rnnt_loss_fwd_bwd(const void *logits, const int64_t sizes[4], const int64_t strides[4],
+                          int dtype, const int64_t *labels, const int64_t *logit_lens,
+                          const int64_t *label_lens, int blank, double sigma, int reduction,
+                          float *loss_out, void *grad_out, void *stream) {
+  tdt::Problem p;
+  int rc = tdt::validate(logits, sizes, strides, dtype, labels, logit_lens, label_lens, nullptr,
+                         0, blank, sigma, reduction, loss_out, grad_out, &p, true, true);
+  if (rc != TDT_OK) return rc;
+  tdt::Layout L;
+  if (!tdt::make_layout(sizes, p.n_dur, &L)) return TDT_ERR_BAD_SIZES;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   void *ws_ptr = nullptr;
   if (cudaMallocAsync(&ws_ptr, L.total, s) != cudaSuccess) return TDT_ERR_CUDA;

@@ -45,12 +45,12 @@ enum Reduction { kNone = 0, kSum = 1, kMean = 2, kMeanBatch = 3, kMeanVolume = 4
 // Everything a kernel needs to know about one call.  Passed by value.
 struct Problem {
   const void *logits;
-  long long B, T, U1, VD, V, D;   // U1 = U + 1
+  long long B, T, U1, VD, V, D;   // U1 = U + 1; D: duration logits per row
   long long s0, s1, s2;           // element strides of logits (s3 == 1)
   const long long *labels;        // [B, U1-1]
   const long long *logit_lens;    // [B]
   const long long *label_lens;    // [B]
-  int dur[kMaxDurations];
+  int dur[kMaxDurations];         // lattice durations
   int n_dur;
   int max_dur;
   int blank;
@@ -59,6 +59,9 @@ struct Problem {
   long long n_diag;               // T + U1 - 1 anti-diagonals per utterance
   int rc_stride;                  // floats per row-coefficient record
   int rec_len;                    // fx values per node arc record (arc_record_len)
+  int rnnt;                       // 1: plain RNN-T: no duration logits (D = 0); the
+                                  //    lattice durations are {0, 1} with blank arcs
+                                  //    of duration 1 and label arcs of duration 0 only
 };
 
 // Node arc record (fx values), one per lattice node in anti-diagonal order:
@@ -236,7 +239,8 @@ Workspace carve(const Layout &L, void *base);
 int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4], int dtype,
              const int64_t *labels, const int64_t *logit_lens, const int64_t *label_lens,
              const int32_t *durations, int n_dur, int blank, double sigma, int reduction,
-             const float *loss_out, const void *grad_out, Problem *p, bool need_loss);
+             const float *loss_out, const void *grad_out, Problem *p, bool need_loss,
+             bool rnnt = false);
 
 // ---- launchers (one per translation unit) ----------------------------------
 // Rows are flat node ids n in [n_begin, n_end); utterances b in [b_begin, b_end).

@@ -178,25 +178,34 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
   group_ms<TPR>(md, sd, sm_m, sm_s);
   if (!active) return;
   const fx_t lse_fx = fx_from_float(M) + fx_log_ge1(S);
-  const fx_t lsed_fx = fx_from_float(md) + fx_log_ge1(sd);
 
-  // the node's arc record: [i] blank arc with duration i, [D + i] label arc
-  // with duration i (token log-prob - sigma + duration log-prob)
+  // the node's arc record: [i] blank arc with duration i, [n_dur + i] label
+  // arc with duration i (token log-prob - sigma + duration log-prob)
   const fx_t wbs = clamp_lp(fx_from_float(zb) - lse_fx) - p.sigma_fx;
   const fx_t wls = y_ok ? clamp_lp(fx_from_float(zy) - lse_fx) - p.sigma_fx : 0;
   fx_t *rec = ws.arcw + diag_index(p, b, t, u) * p.rec_len;
+  if (p.rnnt) {
+    // plain RNN-T: no duration head; the blank arc advances one frame, the
+    // label arc none; the other arcs of the lattice's {0, 1} get no weight
+    if (lt < p.n_dur) {
+      rec[lt] = p.dur[lt] == 1 ? wbs : kFxVeryNeg;
+      rec[p.n_dur + lt] = p.dur[lt] == 0 ? wls : kFxVeryNeg;
+    }
+  } else {
+    const fx_t lsed_fx = fx_from_float(md) + fx_log_ge1(sd);
 #pragma unroll
-  for (int c = 0; c < kDurPerLane; ++c) {
-    const int i = lt + c * TPR;
-    if (i < p.D) {
-      const fx_t ld = clamp_lp(fx_from_float(zd[c]) - lsed_fx);
-      rec[i] = wbs + ld;
-      rec[p.D + i] = wls + ld;
+    for (int c = 0; c < kDurPerLane; ++c) {
+      const int i = lt + c * TPR;
+      if (i < p.D) {
+        const fx_t ld = clamp_lp(fx_from_float(zd[c]) - lsed_fx);
+        rec[i] = wbs + ld;
+        rec[p.n_dur + i] = wls + ld;
+      }
     }
   }
   if (lt == 0) {
     ws.lse_tok[n] = M + logf(S);
-    ws.lse_dur[n] = md + logf(sd);
+    ws.lse_dur[n] = p.D > 0 ? md + logf(sd) : 0.0f;
   }
 }
 

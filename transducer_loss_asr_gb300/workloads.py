@@ -48,6 +48,7 @@ class Workload:
     U_range: tuple | None = None
     base_vd: int | None = None     # width of the wider tensor the input is sliced from
     seed: int = BASE_SEED
+    loss: str = "tdt"              # "tdt" | "rnnt" (plain RNN-T: no duration head)
     notes: str = field(default="", compare=False)
 
     @property
@@ -85,6 +86,10 @@ WORKLOADS = {
         "long_labels", B=1, T=2000, U=1200, V=129, blank=128, durations=tuple(range(9)),
         dtype="f32", std=1.0, sigma=0.02, reduction="none", seed=BASE_SEED + 4,
         notes="B1 T2000 U1200 V129 D9 fp32: labels beyond 1024, long float64 lattice"),
+    "parakeet_rnnt": Workload(
+        "parakeet_rnnt", B=4, T=200, U=40, V=8193, blank=8192, durations=(), dtype="f32",
+        std=1.0, sigma=0.0, reduction="mean_volume", seed=BASE_SEED + 5, loss="rnnt",
+        notes="plain RNN-T loss (no duration head) at the pages' benchmark size [4,200,41,8193]"),
 }
 
 TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
