@@ -211,6 +211,56 @@ def run_reference(args, w):
     return 0
 
 
+def run_decode(args, w, inp, dev, world, rank, dist):
+    """Time greedy TDT decoding of the workload's logits (one call = the
+    whole batch).  Each step of an utterance is a dependent row read plus a
+    block-wide argmax, so the call is latency-bound: reported in ms and in
+    decoded tokens per second."""
+    from transducer_loss_asr_gb300 import binding
+
+    def step():
+        return binding.tdt_greedy_decode(inp["logits"], inp["logit_lens"], inp["durations"],
+                                         inp["blank"], args.max_symbols)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        n = step()[0]
+    torch.cuda.synchronize()
+    tokens = int(n.sum().item())
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)
+        starts[i].record()
+        step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    if rank == 0:
+        print(json.dumps({
+            "metric": "greedy TDT decode of precomputed joint outputs, ms per batch",
+            "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": dict(config_dict(w, "flushed between timed steps (2x L2 write)"),
+                           max_symbols=args.max_symbols),
+            "tokens_per_batch": tokens, "tokens_per_s": world * tokens / (ms / 1e3),
+            "roofline": {"bound": "latency", "note": "one dependent row read and block argmax "
+                         "per step; T_b + U + 1 steps at most per utterance"},
+            "gpu_launches": args.steps}))
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def config_dict(w, l2):
     return {"workload": "%s: B%d T%d U%d V%d D%d %s [%d,%d,%d,%d]%s, sigma %g, %s" % (
         w.name, w.B, w.T, w.U, w.V, w.D, w.dtype, w.B, w.T, w.U + 1, w.VD,
@@ -233,6 +283,10 @@ def main():
                     help="override B (smaller profiling cases; not a bench line)")
     ap.add_argument("--frames", type=int, default=None,
                     help="override T (smaller profiling cases; not a bench line)")
+    ap.add_argument("--op", default="loss", choices=["loss", "decode"],
+                    help="loss: TDT loss fwd+bwd (the benchmark); decode: greedy TDT decoding "
+                         "of the workload's logits (a separate measurement)")
+    ap.add_argument("--max-symbols", type=int, default=10)
     ap.add_argument("--lattice-bands", type=int, default=0,
                     help="force K row bands per utterance in the lattice passes (0: automatic)")
     args = ap.parse_args()
@@ -269,6 +323,8 @@ def main():
 
     binding.tdt_loss_set_lattice_bands(args.lattice_bands)
     inp = make_inputs(w, device=dev, seed=w.seed + rank)
+    if args.op == "decode":
+        return run_decode(args, w, inp, dev, world, rank, dist)
     logits = inp["logits"]
     read_b, write_b, valid_rows, all_rows = algorithmic_bytes(inp)
     step_bytes = read_b + write_b

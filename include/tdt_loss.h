@@ -131,6 +131,31 @@ int tdt_rnnt_loss_fwd_bwd(const void *logits, const int64_t sizes[4], const int6
                           float *loss_out, void *grad_out, void *stream);
 
 /*
+ * Greedy TDT decoding over precomputed joint outputs ("Add TDT loss kernel",
+ * transformers PR #46048, commit list: greedy TDT decoding with per-token
+ * timestamps and token durations, and a max_symbols_per_step guard).  With
+ * the joint output z[b,t,u,:] given for every frame t and decoder state u
+ * (u tokens emitted), utterance b is decoded by the walk: start at (0,0);
+ * at (t,u) take k = first argmax of z[0:V) and d = durations[first argmax of
+ * z[V:V+D)]; a token k != blank is emitted with frame t and duration d and
+ * u advances (decoding stops when row u would exceed U); a blank, or any
+ * token once max_symbols tokens were emitted at this frame, moves at least
+ * one frame; otherwise t advances by d; decoding stops at t >= T_b.
+ *   logits, sizes, strides, dtype, logit_lens, durations, n_dur, blank:
+ *             as for tdt_loss_fwd_bwd (no labels);
+ *   max_symbols  >= 1;
+ *   n_out          device int32 [B]: tokens decoded for each utterance;
+ *   tokens_out, frames_out, durations_out  device int32 [B, U+1]: token,
+ *             frame of emission and predicted duration, -1 past n_out[b].
+ * An utterance with T_b < 1 or T_b > T decodes to nothing.  Ties go to the
+ * smallest index; logits are expected to be finite.
+ */
+int tdt_greedy_decode(const void *logits, const int64_t sizes[4], const int64_t strides[4],
+                      int dtype, const int64_t *logit_lens, const int32_t *durations, int n_dur,
+                      int blank, int max_symbols, int32_t *n_out, int32_t *tokens_out,
+                      int32_t *frames_out, int32_t *durations_out, void *stream);
+
+/*
  * Bytes of device scratch that tdt_loss_fwd_bwd_ws needs for these sizes
  * (0 for invalid arguments).  The value depends only on sizes and n_dur.
  */

@@ -221,3 +221,24 @@ def test_rnnt_entry_validates(lib):
     assert call(ok_sizes, ok_strides, sigma=float("inf")) == -8
     assert call(ok_sizes, [150, 30, 10, 2]) == -3
     assert call(ok_sizes, ok_strides, grad=ctypes.c_void_p(FAKE + 4)) == -13
+
+
+def test_greedy_decode_validates(lib):
+    so = lib.lib
+    f = ctypes.c_void_p(FAKE)
+    durs = (ctypes.c_int32 * 3)(0, 1, 2)
+
+    def call(sizes=(2, 5, 3, 10), strides=(150, 30, 10, 1), dtype=0, n_dur=3, blank=6,
+             max_sym=4, logits=FAKE):
+        return so.tdt_greedy_decode(ctypes.c_void_p(logits), (ctypes.c_int64 * 4)(*sizes),
+                                    (ctypes.c_int64 * 4)(*strides), dtype, f, durs, n_dur,
+                                    blank, max_sym, f, f, f, f, None)
+
+    assert call(blank=7) == -6           # V = 10 - 3
+    assert call(max_sym=0) == -2
+    assert call(n_dur=0) == -5
+    assert call(dtype=4) == -4
+    assert call(sizes=(2, 0, 3, 10)) == -2
+    assert call(strides=(150, 30, 10, 3)) == -3
+    assert call(logits=FAKE + 2) == -11
+    assert call(sizes=(0, 5, 3, 10)) == 0  # empty batch: nothing to do, nothing touched

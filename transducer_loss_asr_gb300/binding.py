@@ -46,6 +46,8 @@ def _load() -> ctypes.CDLL:
     lib.tdt_loss_fwd_bwd_noalloc.argtypes = common + [P]
     lib.tdt_rnnt_loss_fwd_bwd.restype = I
     lib.tdt_rnnt_loss_fwd_bwd.argtypes = [P, P, P, I, P, P, P, I, ctypes.c_double, I, P, P, P]
+    lib.tdt_greedy_decode.restype = I
+    lib.tdt_greedy_decode.argtypes = [P, P, P, I, P, P, I, I, I, P, P, P, P, P]
     lib.tdt_loss_fwd.restype = I
     lib.tdt_loss_fwd.argtypes = common[:-1] + [P, ctypes.c_size_t, P]
     lib.tdt_loss_bwd.restype = I
@@ -150,6 +152,29 @@ def tdt_rnnt_loss_fwd_bwd(logits, labels, logit_lens, label_lens, blank, sigma=0
     with torch.cuda.device(logits.device):
         _check(lib.tdt_rnnt_loss_fwd_bwd(*rargs, _stream_handle(logits.device)))
     return loss_out, grad_out
+
+
+def tdt_greedy_decode(logits, logit_lens, durations, blank, max_symbols=10):
+    """Greedy TDT decoding of joint outputs ``logits`` [B, T, U+1, V+D] on the
+    current CUDA stream.  Returns (n [B], tokens, frames, token_durations
+    [B, U+1]) as int32 CUDA tensors, -1 past n[b]."""
+    if logits.dim() != 4:
+        raise ValueError("logits must be [B, T, U+1, V+D]")
+    if logits.dtype not in DTYPES:
+        raise TypeError("logits dtype must be float32, float16 or bfloat16")
+    if logit_lens.dtype != torch.int64 or logit_lens.device != logits.device:
+        raise ValueError("logit_lens must be an int64 tensor on %s" % logits.device)
+    B, _, U1, _ = logits.shape
+    dev = logits.device
+    n = torch.empty(B, dtype=torch.int32, device=dev)
+    tok, frm, dur = (torch.empty(B, U1, dtype=torch.int32, device=dev) for _ in range(3))
+    durs = (ctypes.c_int32 * len(durations))(*[int(d) for d in durations])
+    with torch.cuda.device(dev):
+        _check(lib.tdt_greedy_decode(
+            _ptr(logits), _i64(logits.shape), _i64(logits.stride()), DTYPES[logits.dtype],
+            _ptr(logit_lens.contiguous()), durs, len(durations), int(blank), int(max_symbols),
+            _ptr(n), _ptr(tok), _ptr(frm), _ptr(dur), _stream_handle(dev)))
+    return n, tok, frm, dur
 
 
 def tdt_loss_fwd_bwd_ws(logits, labels, logit_lens, label_lens, durations, blank, workspace,
