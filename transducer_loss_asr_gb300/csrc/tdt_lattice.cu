@@ -306,9 +306,12 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N> __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
-// Diagonals of arc records copied ahead of use: at ~0.5-1 us per diagonal
-// this covers the L2/HBM latency several times over.
+// Diagonals of arc records copied ahead of use: kPrefetchDeep when the
+// record ring fits (single band), else kPrefetch.  At ~0.5-1 us per
+// diagonal either covers the L2/HBM latency; the deeper one also covers it
+// while the streaming passes load HBM.
 constexpr int kPrefetch = 4;
+constexpr int kPrefetchDeep = 8;
 
 // ---- cluster / mbarrier primitives (PTX ISA: mbarrier, mapa, barrier.cluster)
 __device__ __forceinline__ unsigned smem_u32(const void *p) {
@@ -396,6 +399,7 @@ struct ClusterPlan {
   int Rc;       // lattice rows per CTA
   int G;        // lanes per node
   int RA, RW;   // slots of the value ring and of the record ring (powers of two)
+  int P;        // prefetch distance in diagonals (kPrefetchDeep or kPrefetch)
   int threads;  // (Rc + 1) * G rounded up to whole warps, plus a control warp if K > 1
   size_t smem;  // shared bytes used
 };
@@ -509,7 +513,7 @@ struct Band {
 // j - RA before storing.  The control warp issues no copies, no global
 // stores and no compute.
 
-template <int ND, int G, bool MULTI>
+template <int ND, int G, bool MULTI, int P>
 __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace &ws,
                                               const ClusterRings<2 * ND> r, const ClusterPlan cp,
                                               const Band bd, long long b) {
@@ -530,7 +534,6 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     dd[j] = di[j] < ND ? p.dur[di[j]] : -1;
   }
   const int nsteps = bd.Tb + bd.Ub;
-  constexpr int P = kPrefetch;
   const bool pref = row <= cp.Rc && !(MULTI && bd.control_warp);
   const bool producer = upper && row == cp.Rc && k == 0;  // feeds the upper band
   int failed = 0;  // a bounded wait of this thread gave up
@@ -595,7 +598,7 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
   }
 }
 
-template <int ND, int G, bool MULTI>
+template <int ND, int G, bool MULTI, int P>
 __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &ws,
                                              const ClusterRings<2 * ND> r, const ClusterPlan cp,
                                              const Band bd, long long b) {
@@ -617,7 +620,6 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
   }
   const int nsteps = bd.Tb + bd.Ub;
   const int last = nsteps - 1;
-  constexpr int P = kPrefetch;
   const bool pref = own && !(MULTI && bd.control_warp);
   const bool producer = lower && row == 1 && k == 0;  // feeds the lower band
   int failed = 0;  // a bounded wait of this thread gave up
@@ -704,7 +706,7 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
 
 // Block: (Rc + 1) * G compute threads (rounded up to whole warps), then one
 // control warp when there are neighbouring bands.
-template <int ND, int G, bool MULTI>
+template <int ND, int G, bool MULTI, int P>
 __global__ void __launch_bounds__(kLatticeMaxThreads, 1)
 lattice_cluster_kernel(Problem p, Workspace ws, long long b0, ClusterPlan cp) {
   constexpr int REC = 2 * ND;
@@ -753,8 +755,8 @@ lattice_cluster_kernel(Problem p, Workspace ws, long long b0, ClusterPlan cp) {
   bd.Ub = (int)p.label_lens[b];
   bd.U1 = (int)p.U1;
   bd.abort = &s_abort;
-  if (!is_beta) alpha_cluster<ND, G, MULTI>(p, ws, r, cp, bd, b);
-  else beta_cluster<ND, G, MULTI>(p, ws, r, cp, bd, b);
+  if (!is_beta) alpha_cluster<ND, G, MULTI, P>(p, ws, r, cp, bd, b);
+  else beta_cluster<ND, G, MULTI, P>(p, ws, r, cp, bd, b);
   __syncthreads();
   if (MULTI && s_abort && threadIdx.x == 0) ws.usable[b] = 0;  // a wait timed out: NaN loss
   // no band leaves while a neighbour may still write into its shared memory
@@ -791,24 +793,24 @@ bool cluster_plan(const Problem &p, int K, ClusterPlan *cp) {
   // value ring: max_dur + 2 diagonals in use, the rest is how far a band may
   // run ahead of the band it feeds
   const int RA = pow2_at_least(p.max_dur + 10);
-  const int RW = pow2_at_least(kPrefetch + p.max_dur + 3);
-  const size_t bytes = cluster_smem_bytes(RA, RW, Rc, rec);
-  if (bytes > kClusterSmemMax) return false;
-  cp->K = K;
-  cp->Rc = Rc;
-  cp->G = G;
-  cp->RA = RA;
-  cp->RW = RW;
-  cp->threads = threads;
-  cp->smem = bytes;
-  return true;
+  // the deeper prefetch for a single band when its record ring still fits
+  for (int P : {K == 1 ? kPrefetchDeep : kPrefetch, kPrefetch}) {
+    const int RW = pow2_at_least(P + p.max_dur + 3);
+    const size_t bytes = cluster_smem_bytes(RA, RW, Rc, rec);
+    if (bytes > kClusterSmemMax) continue;
+    cp->K = K;
+    cp->Rc = Rc;
+    cp->G = G;
+    cp->RA = RA;
+    cp->RW = RW;
+    cp->P = P;
+    cp->threads = threads;
+    cp->smem = bytes;
+    return true;
+  }
+  return false;
 }
 
-// The fewest bands that fit: a diagonal step is latency-bound, so more bands
-// do not make it shorter, while the exchange between bands costs a share of
-// every step and each band takes an SM from the streaming passes.  One band
-// holds up to 1024 / G threads' worth of rows; then the shared-memory rings
-// decide (cluster_plan).
 int preferred_bands(const Problem &p) {
   const int forced = g_forced_bands.load();
   if (forced > 0) return forced < kMaxCluster ? forced : kMaxCluster;
@@ -820,7 +822,9 @@ cudaError_t launch_cluster_g(const Problem &p, const Workspace &ws, long long b0
                              bool with_beta, const ClusterPlan &cp, cudaStream_t stream,
                              bool *placed) {
   *placed = false;
-  auto kern = cp.K == 1 ? lattice_cluster_kernel<ND, G, false> : lattice_cluster_kernel<ND, G, true>;
+  auto kern = cp.K > 1 ? lattice_cluster_kernel<ND, G, true, kPrefetch>
+                       : (cp.P == kPrefetchDeep ? lattice_cluster_kernel<ND, G, false, kPrefetchDeep>
+                                                : lattice_cluster_kernel<ND, G, false, kPrefetch>);
   // at least kLatticeSmemFloor, so no node-table or gradient block shares the SM
   const size_t bytes = cp.smem < (size_t)kLatticeSmemFloor ? (size_t)kLatticeSmemFloor : cp.smem;
   cudaError_t e =
