@@ -35,6 +35,7 @@
 #include <mutex>
 #include <tuple>
 
+#include "tdt_async.cuh"
 #include "tdt_common.cuh"
 
 namespace tdt {
@@ -298,14 +299,6 @@ beta_kernel(Problem p, Workspace ws, long long b0) {
 
 // ---------------------------------------------------------------- cluster variant
 
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N> __device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
-}
 // Diagonals of arc records copied ahead of use: kPrefetchDeep when the
 // record ring fits (single band), else kPrefetch.  At ~0.5-1 us per
 // diagonal either covers the L2/HBM latency; the deeper one also covers it
@@ -313,10 +306,8 @@ template <int N> __device__ __forceinline__ void cp_async_wait() {
 constexpr int kPrefetch = 4;
 constexpr int kPrefetchDeep = 8;
 
-// ---- cluster / mbarrier primitives (PTX ISA: mbarrier, mapa, barrier.cluster)
-__device__ __forceinline__ unsigned smem_u32(const void *p) {
-  return (unsigned)__cvta_generic_to_shared(p);
-}
+// ---- cluster primitives (PTX ISA: mapa, barrier.cluster, st.async); the
+// copy and mbarrier helpers are in tdt_async.cuh
 __device__ __forceinline__ unsigned cluster_rank() {
   unsigned r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -325,13 +316,6 @@ __device__ __forceinline__ unsigned cluster_rank() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                ::: "memory");
-}
-__device__ __forceinline__ void mbar_init(unsigned long long *bar, unsigned count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-               : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init_cluster() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 // Shared-memory address, in CTA `cta` of the cluster, of the local object at p.
 __device__ __forceinline__ unsigned map_cta(const void *p, unsigned cta) {
@@ -350,12 +334,6 @@ __device__ __forceinline__ void st_async_lv(unsigned addr, const LV &v, unsigned
       "r"(__float_as_uint(v.s)), "r"(__float_as_uint(v.pad)), "r"(bar_addr)
       : "memory");
 }
-// Arrive on a local mbarrier and expect `bytes` more transaction bytes this phase.
-__device__ __forceinline__ void arrive_expect_tx(unsigned long long *bar, unsigned bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
 // Arrive on an mbarrier of another CTA of the cluster, relaxed: used only
 // to say "slot consumed", after a CTA barrier that every reader of the slot
 // reached with its loads of the slot already returned (their values feed
@@ -365,30 +343,6 @@ __device__ __forceinline__ void arrive_cluster_relaxed(unsigned bar_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr)
                : "memory");
 }
-// Non-blocking probe of a phase (test_wait never suspends the thread, so a
-// completion signalled from another SM is seen at the next probe).
-__device__ __forceinline__ bool test_wait_parity(unsigned long long *bar, unsigned parity) {
-  unsigned ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// About one second at the GB300 clock: far beyond any legitimate wait.
-constexpr long long kWaitLimitCycles = 2000000000LL;
-// Wait for the completion of the phase of parity `parity`; false on timeout.
-__device__ __forceinline__ bool wait_parity_bounded(unsigned long long *bar, unsigned parity) {
-  if (test_wait_parity(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (!test_wait_parity(bar, parity))
-    if (clock64() - t0 > kWaitLimitCycles) return false;
-  return true;
-}
-
 // Lanes per node: one per duration up to 8 (a power of two, so a node's
 // lanes are an aligned part of a warp); 4 lanes of 3 durations for D = 9.
 constexpr int group_lanes(int nd) { return nd <= 1 ? 1 : nd <= 2 ? 2 : nd <= 4 ? 4 : nd <= 8 ? 8 : 4; }

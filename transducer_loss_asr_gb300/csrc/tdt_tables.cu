@@ -72,6 +72,45 @@ __device__ __forceinline__ void group_ms(float &m, float &s, float *sm_m, float 
   }
 }
 
+// Outputs of one usable node from its reduced row: the two log-sum-exps
+// and the arc record -- [i] blank arc with duration i, [n_dur + i] label arc
+// with duration i (token log-prob - sigma + duration log-prob).  Lane lt
+// of the row group holds durations lt, lt + TPR, ... in zd.
+template <int TPR, int DPL>
+__device__ __forceinline__ void write_node_outputs(const Problem &p, const Workspace &ws,
+                                                   long long n, long long b, long long t,
+                                                   long long u, int lt, float M, float S,
+                                                   float md, float sd, const float *zd, float zb,
+                                                   float zy, bool y_ok) {
+  const fx_t lse_fx = fx_from_float(M) + fx_log_ge1(S);
+  const fx_t wbs = clamp_lp(fx_from_float(zb) - lse_fx) - p.sigma_fx;
+  const fx_t wls = y_ok ? clamp_lp(fx_from_float(zy) - lse_fx) - p.sigma_fx : 0;
+  fx_t *rec = ws.arcw + diag_index(p, b, t, u) * p.rec_len;
+  if (p.rnnt) {
+    // plain RNN-T: no duration head; the blank arc advances one frame, the
+    // label arc none; the other arcs of the lattice's {0, 1} get no weight
+    if (lt < p.n_dur) {
+      rec[lt] = p.dur[lt] == 1 ? wbs : kFxVeryNeg;
+      rec[p.n_dur + lt] = p.dur[lt] == 0 ? wls : kFxVeryNeg;
+    }
+  } else {
+    const fx_t lsed_fx = fx_from_float(md) + fx_log_ge1(sd);
+#pragma unroll
+    for (int c = 0; c < DPL; ++c) {
+      const int i = lt + c * TPR;
+      if (i < p.D) {
+        const fx_t ld = clamp_lp(fx_from_float(zd[c]) - lsed_fx);
+        rec[i] = wbs + ld;
+        rec[p.n_dur + i] = wls + ld;
+      }
+    }
+  }
+  if (lt == 0) {
+    ws.lse_tok[n] = M + logf(S);
+    ws.lse_dur[n] = p.D > 0 ? md + logf(sd) : 0.0f;
+  }
+}
+
 template <int DT, int TPR>
 __global__ void __launch_bounds__(kTablesThreads, 4)
 node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) {
@@ -177,36 +216,7 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
   }
   group_ms<TPR>(md, sd, sm_m, sm_s);
   if (!active) return;
-  const fx_t lse_fx = fx_from_float(M) + fx_log_ge1(S);
-
-  // the node's arc record: [i] blank arc with duration i, [n_dur + i] label
-  // arc with duration i (token log-prob - sigma + duration log-prob)
-  const fx_t wbs = clamp_lp(fx_from_float(zb) - lse_fx) - p.sigma_fx;
-  const fx_t wls = y_ok ? clamp_lp(fx_from_float(zy) - lse_fx) - p.sigma_fx : 0;
-  fx_t *rec = ws.arcw + diag_index(p, b, t, u) * p.rec_len;
-  if (p.rnnt) {
-    // plain RNN-T: no duration head; the blank arc advances one frame, the
-    // label arc none; the other arcs of the lattice's {0, 1} get no weight
-    if (lt < p.n_dur) {
-      rec[lt] = p.dur[lt] == 1 ? wbs : kFxVeryNeg;
-      rec[p.n_dur + lt] = p.dur[lt] == 0 ? wls : kFxVeryNeg;
-    }
-  } else {
-    const fx_t lsed_fx = fx_from_float(md) + fx_log_ge1(sd);
-#pragma unroll
-    for (int c = 0; c < kDurPerLane; ++c) {
-      const int i = lt + c * TPR;
-      if (i < p.D) {
-        const fx_t ld = clamp_lp(fx_from_float(zd[c]) - lsed_fx);
-        rec[i] = wbs + ld;
-        rec[p.n_dur + i] = wls + ld;
-      }
-    }
-  }
-  if (lt == 0) {
-    ws.lse_tok[n] = M + logf(S);
-    ws.lse_dur[n] = p.D > 0 ? md + logf(sd) : 0.0f;
-  }
+  write_node_outputs<TPR, kDurPerLane>(p, ws, n, b, t, u, lt, M, S, md, sd, zd, zb, zy, y_ok);
 }
 
 template <int DT, int TPR>
