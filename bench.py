@@ -46,11 +46,11 @@ FALLBACK_HBM_GBS = 6800.0
 # its sources hash to this sha256 (kernel_sha).
 NCU_TRAFFIC = {
     # ncu --set full, one launch = one utterance [1,200,41,8198] fp32 (the
-    # per-launch work of the four-chunk B=4 bench): read 270059008 + written
-    # 209289728 bytes (the rest of the writes retire from L2 after the kernel)
+    # per-launch work of the four-chunk B=4 bench): read 269653504 + written
+    # 209491200 bytes (the rest of the writes retire from L2 after the kernel)
     ("grad", "parakeet"): {
-        "bytes": 270059008 + 209289728,
-        "sha256": "87e685a532848f9e188f93c753b806ba5645d5aa85822dd99ba5f1eec099ee4b",
+        "bytes": 269653504 + 209491200,
+        "sha256": "fc9d7001b6169a363f3fe16da88c8090bc5d477bbfe382bfc95f218666b5db60",
     },
 }
 

@@ -234,11 +234,11 @@ int tdt_loss_fwd_bwd_noalloc(const void *logits, const int64_t sizes[4],
 
 /*
  * Benchmark support (not needed for correctness).  Kernel ids: node tables,
- * lattice (alpha and beta), (unused), reduction, gradient.
+ * lattice (alpha and beta), row coefficients, reduction, gradient.
  */
 #define TDT_KERNEL_TABLES 0
 #define TDT_KERNEL_LATTICE 1
-#define TDT_KERNEL_UNUSED 2
+#define TDT_KERNEL_COEFFS 2
 #define TDT_KERNEL_REDUCE 3
 #define TDT_KERNEL_GRAD 4
 #define TDT_KERNEL_COUNT 5

@@ -278,7 +278,7 @@ def tdt_loss_set_lattice_bands(bands: int) -> int:
     return int(lib.tdt_loss_set_lattice_bands(int(bands)))
 
 
-KERNEL_NAMES = ("node_tables", "lattice", "unused", "reduce", "grad")
+KERNEL_NAMES = ("node_tables", "lattice", "row_coeffs", "reduce", "grad")
 
 
 def tdt_loss_timing_enable(on: bool) -> None:

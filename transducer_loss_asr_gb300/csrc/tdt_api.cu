@@ -266,7 +266,10 @@ int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void 
     TDT_TRY(cudaStreamWaitEvent(side, res->tables_done[c], 0));
     TDT_TRY(timed(TDT_KERNEL_LATTICE, side,
                   [&] { return launch_lattice(p, ws, b0, b1, coeffs, side); }));
-    if (coeffs) TDT_TRY(launch_row_coeffs(p, ws, b0 * rows_per_utt, b1 * rows_per_utt, side));
+    if (coeffs)
+      TDT_TRY(timed(TDT_KERNEL_COEFFS, side, [&] {
+        return launch_row_coeffs(p, ws, b0 * rows_per_utt, b1 * rows_per_utt, side);
+      }));
     TDT_TRY(cudaEventRecord(res->lattice_done[c], side));
   }
   // the reduction needs every chunk's log-likelihood; it joins all side streams
