@@ -66,6 +66,39 @@ def algorithmic_bytes(inp):
     return valid_rows * w.VD * elt, all_rows * w.VD * elt, valid_rows, all_rows
 
 
+def nominal_hbm_gbs(dev):
+    """HBM bandwidth from the device's memory clock and bus width (double
+    data rate), for context beside the measured copy peak; None if the
+    attributes cannot be read."""
+    prop = torch.cuda.get_device_properties(dev)
+    clk, bus = getattr(prop, "memory_clock_rate", 0), getattr(prop, "memory_bus_width", 0)
+    if not clk or not bus:
+        try:  # the CUDA runtime the library already loaded
+            import ctypes
+
+            rt = None
+            for name in ("libcudart.so.13", "libcudart.so", "/usr/local/cuda/lib64/libcudart.so"):
+                try:
+                    rt = ctypes.CDLL(name)
+                    break
+                except OSError:
+                    continue
+            if rt is None:
+                return None
+            vals = []
+            for attr in (36, 37):  # cudaDevAttrMemoryClockRate (kHz), ...GlobalMemoryBusWidth (bits)
+                v = ctypes.c_int(0)
+                if rt.cudaDeviceGetAttribute(ctypes.byref(v), attr, dev.index or 0) != 0:
+                    return None
+                vals.append(v.value)
+            clk, bus = vals
+        except Exception:
+            return None
+    if not clk or not bus:
+        return None
+    return clk * 1e3 * 2 * bus / 8 / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -472,6 +505,7 @@ def main():
             "dtype": w.dtype, "data": "synthetic",
             "config": config_dict(w, "flushed between timed steps (2x L2 write)"),
             "frac_of_hbm_roofline": step_frac,
+            "nominal_hbm_gbs": nominal_hbm_gbs(dev),
             "algorithmic_bytes_per_step": step_bytes,
             "roofline": roofline,
             "kernels": per_kernel,

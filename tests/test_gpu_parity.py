@@ -299,3 +299,55 @@ def test_lattice_bands_do_not_change_results(binding, oracle_mod, name):
     ref = run_oracle(oracle_mod, inp)
     check_loss(results[0][1], ref.loss, w.dtype)
     check_grad(results[0][2], ref.grad, w.dtype)
+
+
+# ------------------------------------------------------------- CUDA graphs
+
+@pytest.mark.parametrize("own_workspace", [True, False])
+def test_cuda_graph_capture_and_replay(binding, own_workspace):
+    """The call is stream-ordered (the internal lattice streams fork from and
+    join back to the caller's stream through events), so it can be captured
+    into a CUDA graph; replays give the eager results, also after the inputs
+    change in place."""
+    w = scaled(WORKLOADS["tiny"], name="graph", B=3, T=21, U=6, V=200, blank=199,
+               durations=(0, 1, 2, 3, 4), sigma=0.05, reduction="mean_volume",
+               T_range=(10, 21), U_range=(2, 6), seed=606)
+    inp = make_inputs(w, device="cuda")
+    z = inp["logits"]
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    grad = torch.empty_like(z)
+    ws = torch.empty(binding.workspace_size(z.shape, len(inp["durations"])), dtype=torch.uint8,
+                     device="cuda")
+    args = (z, inp["labels"], inp["logit_lens"], inp["label_lens"], inp["durations"],
+            inp["blank"])
+
+    def call():
+        if own_workspace:
+            binding.tdt_loss_fwd_bwd_ws(*args, ws, sigma=inp["sigma"], reduction="mean_volume",
+                                        loss_out=loss, grad_out=grad)
+        else:
+            binding.tdt_loss_fwd_bwd(*args, inp["sigma"], "mean_volume", loss_out=loss,
+                                     grad_out=grad)
+
+    call()  # eager first: creates the library's streams and sets kernel attributes
+    torch.cuda.synchronize()
+    ref_loss, ref_grad = loss.clone(), grad.clone()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    loss.zero_()
+    grad.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(loss, ref_loss) and torch.equal(grad, ref_grad)
+    # new values in the captured input buffer: the replay computes them
+    z.mul_(1.5)
+    call()
+    torch.cuda.synchronize()
+    eager_loss, eager_grad = loss.clone(), grad.clone()
+    loss.zero_()
+    grad.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(loss, eager_loss) and torch.equal(grad, eager_grad)
+    assert not torch.equal(eager_loss, ref_loss)
