@@ -458,27 +458,34 @@ def main():
 
     # Roofline of the gradient pass (K4), the largest HBM-bound share of the
     # step; the lattice passes are latency-bound, run on SMs of their own and
-    # overlap K1/K4 (their share is reported beside it).  Per-launch bytes are
-    # the step's algorithmic bytes over the K4 launches of one step.
-    per_kernel = {k: {"ms_per_launch": (ms / n if n else 0.0), "launches": n}
-                  for k, (ms, n) in kt.items()}
+    # overlap K1/K4 (their share is reported beside it).  The K4 launches of a
+    # step (one per chunk) run on two streams and overlap one another's
+    # tails, so K4's time per step is its busy window (first launch start to
+    # last launch end, CUDA events on the launching streams) and the bytes are
+    # the step's algorithmic bytes; per launch, both are divided by the K4
+    # launches per step.
+    per_kernel = {k: {"ms_per_launch": (ms / n if n else 0.0), "launches": n,
+                      "busy_ms_per_step": span / args.steps}
+                  for k, (ms, n, span) in kt.items()}
     peak, peak_kind = measured_peaks()
     roofline = None
-    ms_g, n_g = kt.get("grad", (0.0, 0))
-    if n_g:
+    ms_g, n_g, span_g = kt.get("grad", (0.0, 0, 0.0))
+    if n_g and span_g > 0:
         per_step = n_g / args.steps
         bytes_launch = (read_b + write_b) / per_step
-        achieved = bytes_launch / (ms_g / n_g / 1e3) / 1e9
+        achieved = (read_b + write_b) * args.steps / (span_g / 1e3) / 1e9
         tr = NCU_TRAFFIC.get(("grad", w.name))
         traffic = tr["bytes"] if tr and tr["sha256"] == kernel_sha("grad") else None
         roofline = {"bound": "hbm", "kernel": "grad", "achieved": achieved, "peak": peak,
                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                     "algorithmic_bytes_per_launch": bytes_launch,
+                    "launches_per_step": per_step,
+                    "time": "K4 busy window per step / launches per step",
                     "peak_source": peak_kind + " hbm_gbs (copy)"}
-    ms_t, n_t = kt.get("node_tables", (0.0, 0))
-    if n_t:
-        per_kernel["node_tables"]["achieved_gbs"] = read_b * args.steps / (ms_t / 1e3) / 1e9
-    if n_g:
+    ms_t, n_t, span_t = kt.get("node_tables", (0.0, 0, 0.0))
+    if n_t and span_t > 0:
+        per_kernel["node_tables"]["achieved_gbs"] = read_b * args.steps / (span_t / 1e3) / 1e9
+    if roofline:
         per_kernel["grad"]["achieved_gbs"] = roofline["achieved"]
     step_frac = (step_bytes / (ms_per_step / 1e3) / 1e9) / peak
 
@@ -509,7 +516,7 @@ def main():
             "algorithmic_bytes_per_step": step_bytes,
             "roofline": roofline,
             "kernels": per_kernel,
-            "gpu_launches": int(sum(n for _, n in kt.values())),
+            "gpu_launches": int(sum(v[1] for v in kt.values())),
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": float(e2e_ms.item()),

@@ -182,8 +182,8 @@ int tdt_loss_fwd_bwd_ws(const void *logits, const int64_t sizes[4], const int64_
  * its ops, torch.compile ("Add TDT loss kernel", transformers PR #46048,
  * review thread on the kernel mapping).
  *
- * tdt_loss_fwd: node tables, alpha, beta, per-row gradient coefficients and
- *   the reduction into loss_out.  workspace as for tdt_loss_fwd_bwd_ws; its
+ * tdt_loss_fwd: node tables, alpha, beta, the arc fractions and the
+ *   reduction into loss_out.  workspace as for tdt_loss_fwd_bwd_ws; its
  *   contents must stay untouched until tdt_loss_bwd has run.
  */
 int tdt_loss_fwd(const void *logits, const int64_t sizes[4], const int64_t strides[4], int dtype,
@@ -234,14 +234,13 @@ int tdt_loss_fwd_bwd_noalloc(const void *logits, const int64_t sizes[4],
 
 /*
  * Benchmark support (not needed for correctness).  Kernel ids: node tables,
- * lattice (alpha and beta), row coefficients, reduction, gradient.
+ * lattice (alpha and beta), reduction, gradient.
  */
 #define TDT_KERNEL_TABLES 0
 #define TDT_KERNEL_LATTICE 1
-#define TDT_KERNEL_COEFFS 2
-#define TDT_KERNEL_REDUCE 3
-#define TDT_KERNEL_GRAD 4
-#define TDT_KERNEL_COUNT 5
+#define TDT_KERNEL_REDUCE 2
+#define TDT_KERNEL_GRAD 3
+#define TDT_KERNEL_COUNT 4
 
 /*
  * on != 0: every later call records a CUDA event pair around each of its
@@ -251,13 +250,18 @@ int tdt_loss_fwd_bwd_noalloc(const void *logits, const int64_t sizes[4],
 void tdt_loss_timing_enable(int on);
 
 /*
- * Sum of the recorded kernel durations in milliseconds (ms_out) and the
- * number of launches (count_out) per kernel id, for the first n ids, since
- * the last reset.  Blocks until the recorded events have completed.
- * reset != 0 clears the sums afterwards.  Returns the number of ids written
- * or TDT_ERR_CUDA.
+ * Per kernel id, for the first n ids, since the last reset: the sum of the
+ * recorded launch durations in milliseconds (ms_out), the number of launches
+ * (count_out), and the sum over calls of the kernel's busy window in the
+ * call (span_ms_out): from the start of its first launch to the end of its
+ * last launch in that call.  Launches of one kernel run on several streams
+ * and may overlap, so span_ms_out can be less than ms_out.  Any output may
+ * be NULL.  Blocks until the recorded events have completed.  reset != 0
+ * clears the sums afterwards.  Returns the number of ids written or
+ * TDT_ERR_CUDA.  Timing assumes one host thread making calls.
  */
-int tdt_loss_timing_read(double *ms_out, int64_t *count_out, int n, int reset);
+int tdt_loss_timing_read(double *ms_out, int64_t *count_out, double *span_ms_out, int n,
+                         int reset);
 
 /*
  * Tuning and testing support.  The lattice passes split an utterance's rows

@@ -4,8 +4,8 @@ The loss is registered as two custom ops over the split C ABI
 (``tdt_loss_fwd`` / ``tdt_loss_bwd`` in include/tdt_loss.h):
 
 * ``tdt_gb300::tdt_loss_forward`` -> (loss, workspace): node tables, alpha,
-  beta and the per-row gradient coefficients; the workspace (uint8) carries
-  them to the backward op.
+  beta and the arc fractions; the workspace (uint8) carries them to the
+  backward op.
 * ``tdt_gb300::tdt_loss_backward`` -> grad: the gradient pass only, scaled by
   the upstream gradient of the loss, so an arbitrary ``grad_output`` costs no
   extra pass over the gradient.
@@ -37,17 +37,15 @@ def workspace_nbytes(B, T, U1, n_dur):
     The same value as the C ABI's tdt_loss_workspace_size, written with
     integer arithmetic only so that it also holds for symbolic sizes under
     torch.compile: per anti-diagonal slot a node arc record of 2 * D
-    fixed-point values, alpha and beta (16 bytes each);
-    per node two log-sum-exps, a row-coefficient record and 2 + D arc
-    fractions; per utterance log-likelihood, scale and flag; every region
-    256-byte aligned.
+    fixed-point values, alpha and beta (16 bytes each); per node two
+    log-sum-exps and 2 + D arc fractions; per utterance log-likelihood, scale
+    and flag; every region 256-byte aligned.
     """
     ndiag = B * (T + U1 - 1) * U1
     nodes = B * T * U1
-    rc_stride = (8 + n_dur + 3) // 4 * 4
     rec_len = 2 * n_dur
     regions = (ndiag * 8 * rec_len, ndiag * 16, ndiag * 16, nodes * 4, nodes * 4,
-               nodes * 4 * rc_stride, nodes * 4 * (2 + n_dur), B * 16, B * 8, B * 4)
+               nodes * 4 * (2 + n_dur), B * 16, B * 8, B * 4)
     off = 0
     for r in regions:
         off = _align(off + r)

@@ -63,7 +63,7 @@ def _load() -> ctypes.CDLL:
     lib.tdt_loss_timing_enable.restype = None
     lib.tdt_loss_timing_enable.argtypes = [I]
     lib.tdt_loss_timing_read.restype = I
-    lib.tdt_loss_timing_read.argtypes = [P, P, I, I]
+    lib.tdt_loss_timing_read.argtypes = [P, P, P, I, I]
     return lib
 
 
@@ -278,7 +278,7 @@ def tdt_loss_set_lattice_bands(bands: int) -> int:
     return int(lib.tdt_loss_set_lattice_bands(int(bands)))
 
 
-KERNEL_NAMES = ("node_tables", "lattice", "row_coeffs", "reduce", "grad")
+KERNEL_NAMES = ("node_tables", "lattice", "reduce", "grad")
 
 
 def tdt_loss_timing_enable(on: bool) -> None:
@@ -287,11 +287,15 @@ def tdt_loss_timing_enable(on: bool) -> None:
 
 
 def tdt_loss_timing_read(reset: bool = True):
-    """{kernel name: (summed ms, launches)} since the last reset; waits for the events."""
+    """{kernel name: (summed ms, launches, summed busy-window ms)} since the
+    last reset; waits for the events.  The busy window of a kernel in one call
+    runs from the start of its first launch to the end of its last (launches
+    on several streams may overlap)."""
     n = len(KERNEL_NAMES)
     ms = (ctypes.c_double * n)()
     cnt = (ctypes.c_int64 * n)()
-    rc = lib.tdt_loss_timing_read(ms, cnt, n, 1 if reset else 0)
+    span = (ctypes.c_double * n)()
+    rc = lib.tdt_loss_timing_read(ms, cnt, span, n, 1 if reset else 0)
     if rc < 0:
         raise TDTError(rc, status_string(rc))
-    return {KERNEL_NAMES[i]: (ms[i], cnt[i]) for i in range(n)}
+    return {KERNEL_NAMES[i]: (ms[i], cnt[i], span[i]) for i in range(n)}

@@ -1,15 +1,27 @@
 // tdt_api.cu -- the C ABI (include/tdt_loss.h): argument checks, scratch
 // layout, and the order of the kernels.
 //
-// The batch is cut into up to kChunks groups of utterances.  On the caller's
-// stream: K1 node tables for chunk 0, 1, ..., then K4 gradient for chunk 0,
-// 1, ...  On internal high-priority streams (one per chunk): the alpha/beta
-// lattice pass of chunk c as soon as K1 of chunk c is done; then the
-// reduction once every chunk's lattice is done.  K4 of chunk c waits for the
-// lattice of chunk c.  So the latency-bound lattice passes
-// (a few SMs) run under the bandwidth-bound K1/K4 passes of other chunks
-// instead of between them.  The fork and join are CUDA events, so the whole
-// call is stream-ordered (and capturable) on the caller's stream.
+// The batch is cut into up to kChunks groups of utterances, and the call
+// forks from the caller's stream onto internal streams of three priorities:
+//   * highest: one stream per chunk runs the alpha/beta lattice pass of
+//     chunk c as soon as K1 of chunk c is done; the first of them then runs
+//     the reduction once every chunk's lattice is done;
+//   * middle: K1 node tables for chunk 0, 1, ... one after another (each
+//     waits for the end of the one before), on two streams taken in turn.
+//     K1 of chunk 1 also waits until every block of the lattice pass of
+//     chunk 0 has started (a launch-completion event): a lattice block needs
+//     an SM to itself, and once the next K1 pass has filled the GPU it was
+//     measured to wait ~27 us for one.  Only the lattice of chunk 0 is on the
+//     critical path; the later ones end long before their K4 passes start;
+//   * lowest: K4 gradient of chunk c, once the lattice of chunk c is done,
+//     on two streams taken in turn.
+// The latency-bound lattice passes (a few SMs) run under the bandwidth-bound
+// K1/K4 passes of other chunks instead of between them.  The block scheduler
+// prefers pending blocks of higher-priority streams, so a K4 pass that is
+// ready fills the SMs that the tail of the last K1 pass (or of the K4 pass
+// before it) leaves idle instead of waiting for it to end.  The fork and the
+// joins are CUDA events, so the whole call is stream-ordered (and
+// capturable) on the caller's stream.
 #include <math.h>
 #include <string.h>
 
@@ -23,7 +35,6 @@ namespace tdt {
 namespace {
 
 size_t align_up(size_t v) { return (v + 255) & ~(size_t)255; }
-int row_coeff_stride(int n_dur) { return (kRcD + n_dur + 3) & ~3; }
 
 }  // namespace
 
@@ -45,7 +56,6 @@ bool make_layout(const int64_t sizes[4], int n_dur, Layout *L) {
   L->beta = take(ndiag * sizeof(LV));
   L->lse_tok = take(nodes * 4);
   L->lse_dur = take(nodes * 4);
-  L->rowc = take(nodes * 4 * (size_t)row_coeff_stride(n_dur));
   L->frac = take(nodes * 4 * (size_t)(2 + n_dur));
   L->loglik = take((size_t)B * sizeof(LV));
   L->scale = take((size_t)B * 8);
@@ -62,7 +72,6 @@ Workspace carve(const Layout &L, void *base) {
   w.beta = reinterpret_cast<LV *>(c + L.beta);
   w.lse_tok = reinterpret_cast<float *>(c + L.lse_tok);
   w.lse_dur = reinterpret_cast<float *>(c + L.lse_dur);
-  w.rowc = reinterpret_cast<float *>(c + L.rowc);
   w.frac = reinterpret_cast<float *>(c + L.frac);
   w.loglik = reinterpret_cast<LV *>(c + L.loglik);
   w.scale = reinterpret_cast<double *>(c + L.scale);
@@ -142,7 +151,6 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
   p->reduction = reduction;
   p->sigma_fx = (fx_t)llround(sigma * kFxOne);
   p->n_diag = T + U1 - 1;
-  p->rc_stride = row_coeff_stride(n_dur);
   p->rec_len = arc_record_len(n_dur);
   p->rnnt = rnnt ? 1 : 0;
   return TDT_OK;
@@ -151,13 +159,20 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
 namespace {
 
 // ---- optional per-kernel timing (benchmarks) --------------------------------
+// Each call records a reference event on the caller's stream before its first
+// kernel; every timed launch records an event pair on its own stream.  A
+// kernel's busy window in a call runs from the start of its first launch to
+// the end of its last one (launches of one kernel may overlap on several
+// streams), measured from the call's reference event.
 struct Timing {
   std::mutex mu;
   bool on = false;
-  struct Pending { int id; cudaEvent_t a, b; };
+  struct Pending { int id; long long call; cudaEvent_t a, b; };
   std::vector<Pending> pending;
+  std::vector<cudaEvent_t> call_ref;  // reference event of call k (k = index)
   std::vector<cudaEvent_t> pool;
   double ms[TDT_KERNEL_COUNT] = {0};
+  double span[TDT_KERNEL_COUNT] = {0};
   long long count[TDT_KERNEL_COUNT] = {0};
 };
 Timing &timing() {
@@ -175,14 +190,26 @@ cudaEvent_t take_event(Timing &t) {
   return e;
 }
 
+// Start of a call: its reference event, when timing is on.
+void begin_timed_call(cudaStream_t stream) {
+  Timing &t = timing();
+  std::lock_guard<std::mutex> g(t.mu);
+  if (!t.on) return;
+  cudaEvent_t e = take_event(t);
+  cudaEventRecord(e, stream);
+  t.call_ref.push_back(e);
+}
+
 // Launch one kernel through `fn`, bracketed by events when timing is on.
 template <class F>
 cudaError_t timed(int id, cudaStream_t stream, F fn) {
   Timing &t = timing();
   bool on;
+  long long call;
   {
     std::lock_guard<std::mutex> g(t.mu);
-    on = t.on;
+    on = t.on && !t.call_ref.empty();
+    call = (long long)t.call_ref.size() - 1;
   }
   if (!on) return fn();
   cudaEvent_t a, b;
@@ -195,7 +222,7 @@ cudaError_t timed(int id, cudaStream_t stream, F fn) {
   cudaError_t e = fn();
   cudaEventRecord(b, stream);
   std::lock_guard<std::mutex> g(t.mu);
-  t.pending.push_back({id, a, b});
+  t.pending.push_back({id, call, a, b});
   return e;
 }
 
@@ -204,9 +231,11 @@ constexpr int kChunks = 4;
 
 struct DeviceRes {
   bool ready = false;
-  cudaStream_t side[kChunks] = {};  // high priority, one per chunk's lattice pass
-  cudaEvent_t fork = nullptr, join = nullptr;
-  cudaEvent_t tables_done[kChunks] = {}, lattice_done[kChunks] = {};
+  cudaStream_t side[kChunks] = {};  // highest priority, one per chunk's lattice pass
+  cudaStream_t tables[2] = {};      // middle priority: the K1 passes, in turn
+  cudaStream_t grad[2] = {};        // lowest priority: the K4 passes, in turn
+  cudaEvent_t fork = nullptr, join = nullptr, tables_end[2] = {}, grad_end[2] = {};
+  cudaEvent_t tables_done[kChunks] = {}, lattice_done[kChunks] = {}, started[kChunks] = {};
   std::mutex mu;                // one call at a time enqueues on these events
 };
 
@@ -218,25 +247,33 @@ DeviceRes *device_res(int dev) {
   if (!all[dev]) all[dev] = new DeviceRes();  // lives until process exit
   DeviceRes *r = all[dev];
   if (!r->ready) {
-    int lo = 0, hi = 0;
+    int lo = 0, hi = 0;  // least and greatest priority (greatest = smallest number)
     if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return nullptr;
+    const int mid = hi < lo ? hi + 1 : lo;
     for (int c = 0; c < kChunks; ++c)
       if (cudaStreamCreateWithPriority(&r->side[c], cudaStreamNonBlocking, hi) != cudaSuccess)
         return nullptr;
-    bool ok = cudaEventCreateWithFlags(&r->fork, cudaEventDisableTiming) == cudaSuccess &&
-              cudaEventCreateWithFlags(&r->join, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < 2; ++i)
+      if (cudaStreamCreateWithPriority(&r->tables[i], cudaStreamNonBlocking, mid) != cudaSuccess ||
+          cudaStreamCreateWithPriority(&r->grad[i], cudaStreamNonBlocking, lo) != cudaSuccess)
+        return nullptr;
+    bool ok = true;
+    for (cudaEvent_t *e : {&r->fork, &r->join, &r->tables_end[0], &r->tables_end[1],
+                           &r->grad_end[0], &r->grad_end[1]})
+      ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
     for (int c = 0; c < kChunks && ok; ++c)
       ok = cudaEventCreateWithFlags(&r->tables_done[c], cudaEventDisableTiming) == cudaSuccess &&
-           cudaEventCreateWithFlags(&r->lattice_done[c], cudaEventDisableTiming) == cudaSuccess;
+           cudaEventCreateWithFlags(&r->lattice_done[c], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&r->started[c], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) return nullptr;
     r->ready = true;
   }
   return r;
 }
 
-// One loss (+ gradient) call.  coeffs: also run beta and the row
-// coefficients (always when grad_out is given; the forward half of the split
-// API keeps them for the backward half).  gscale: upstream gradient of the
+// One loss (+ gradient) call.  coeffs: also run beta and the arc fractions
+// (always when grad_out is given; the forward half of the split API keeps
+// them for the backward half).  gscale: upstream gradient of the
 // loss (device, NULL = 1).
 int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void *grad_out,
         const float *gscale, bool coeffs, cudaStream_t stream) {
@@ -245,6 +282,7 @@ int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void 
   DeviceRes *res = device_res(dev);
   if (!res) return TDT_ERR_CUDA;
   std::lock_guard<std::mutex> g(res->mu);
+  begin_timed_call(stream);
   const bool with_grad = grad_out != nullptr;
   coeffs = coeffs || with_grad;
   const long long rows_per_utt = p.T * p.U1;
@@ -256,38 +294,51 @@ int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void 
   } while (0)
   TDT_TRY(cudaEventRecord(res->fork, stream));
   for (int c = 0; c < nchunk; ++c) TDT_TRY(cudaStreamWaitEvent(res->side[c], res->fork, 0));
+  const int nts = nchunk < 2 ? nchunk : 2;
+  bool started_used = false;
+  for (int i = 0; i < nts; ++i) TDT_TRY(cudaStreamWaitEvent(res->tables[i], res->fork, 0));
   for (int c = 0; c < nchunk; ++c) {
     const long long b0 = b_lo(c), b1 = b_lo(c + 1);
-    cudaStream_t side = res->side[c];
-    TDT_TRY(timed(TDT_KERNEL_TABLES, stream, [&] {
-      return launch_node_tables(p, dtype, ws, b0 * rows_per_utt, b1 * rows_per_utt, stream);
+    cudaStream_t side = res->side[c], ts = res->tables[c & 1];
+    if (c > 0) TDT_TRY(cudaStreamWaitEvent(ts, res->tables_done[c - 1], 0));
+    if (c == 1 && started_used) TDT_TRY(cudaStreamWaitEvent(ts, res->started[0], 0));
+    TDT_TRY(timed(TDT_KERNEL_TABLES, ts, [&] {
+      return launch_node_tables(p, dtype, ws, b0 * rows_per_utt, b1 * rows_per_utt, ts);
     }));
-    TDT_TRY(cudaEventRecord(res->tables_done[c], stream));
+    TDT_TRY(cudaEventRecord(res->tables_done[c], ts));
     TDT_TRY(cudaStreamWaitEvent(side, res->tables_done[c], 0));
-    TDT_TRY(timed(TDT_KERNEL_LATTICE, side,
-                  [&] { return launch_lattice(p, ws, b0, b1, coeffs, side); }));
-    if (coeffs)
-      TDT_TRY(timed(TDT_KERNEL_COEFFS, side, [&] {
-        return launch_row_coeffs(p, ws, b0 * rows_per_utt, b1 * rows_per_utt, side);
-      }));
+    started_used = false;
+    TDT_TRY(timed(TDT_KERNEL_LATTICE, side, [&] {
+      return launch_lattice(p, ws, b0, b1, coeffs, side,
+                            c == 0 && nchunk > 1 ? res->started[0] : nullptr, &started_used);
+    }));
     TDT_TRY(cudaEventRecord(res->lattice_done[c], side));
   }
+  for (int i = 0; i < nts; ++i) TDT_TRY(cudaEventRecord(res->tables_end[i], res->tables[i]));
   // the reduction needs every chunk's log-likelihood; it joins all side streams
   cudaStream_t side0 = res->side[0];
   for (int c = 1; c < nchunk; ++c) TDT_TRY(cudaStreamWaitEvent(side0, res->lattice_done[c], 0));
   TDT_TRY(timed(TDT_KERNEL_REDUCE, side0, [&] { return launch_reduce(p, ws, loss_out, side0); }));
   TDT_TRY(cudaEventRecord(res->join, side0));
+  for (int i = 0; i < nts; ++i) TDT_TRY(cudaStreamWaitEvent(stream, res->tables_end[i], 0));
+  TDT_TRY(cudaStreamWaitEvent(stream, res->join, 0));
   if (with_grad) {
+    const int ngs = nchunk < 2 ? nchunk : 2;
+    for (int i = 0; i < ngs; ++i) TDT_TRY(cudaStreamWaitEvent(res->grad[i], res->fork, 0));
     for (int c = 0; c < nchunk; ++c) {
       const long long b0 = b_lo(c), b1 = b_lo(c + 1);
-      TDT_TRY(cudaStreamWaitEvent(stream, res->lattice_done[c], 0));
-      TDT_TRY(timed(TDT_KERNEL_GRAD, stream, [&] {
+      cudaStream_t gs = res->grad[c & 1];
+      TDT_TRY(cudaStreamWaitEvent(gs, res->lattice_done[c], 0));
+      TDT_TRY(timed(TDT_KERNEL_GRAD, gs, [&] {
         return launch_grad(p, dtype, ws, grad_out, gscale, b0 * rows_per_utt, b1 * rows_per_utt,
-                           stream);
+                           gs);
       }));
     }
+    for (int i = 0; i < ngs; ++i) {
+      TDT_TRY(cudaEventRecord(res->grad_end[i], res->grad[i]));
+      TDT_TRY(cudaStreamWaitEvent(stream, res->grad_end[i], 0));
+    }
   }
-  TDT_TRY(cudaStreamWaitEvent(stream, res->join, 0));
 #undef TDT_TRY
   return TDT_OK;
 }
@@ -296,6 +347,7 @@ int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void 
 int run_bwd(const Problem &p, int dtype, const Workspace &ws, void *grad_out, const float *gscale,
             cudaStream_t stream) {
   if (p.B == 0) return TDT_OK;
+  begin_timed_call(stream);
   if (timed(TDT_KERNEL_GRAD, stream, [&] {
         return launch_grad(p, dtype, ws, grad_out, gscale, 0, p.B * p.T * p.U1, stream);
       }) != cudaSuccess)
@@ -445,29 +497,45 @@ void tdt_loss_timing_enable(int on) {
   t.on = on != 0;
 }
 
-int tdt_loss_timing_read(double *ms_out, int64_t *count_out, int n, int reset) {
+int tdt_loss_timing_read(double *ms_out, int64_t *count_out, double *span_ms_out, int n,
+                         int reset) {
   tdt::Timing &t = tdt::timing();
   std::lock_guard<std::mutex> g(t.mu);
   int rc = 0;
+  // per call and kernel: earliest start and latest end after the reference
+  std::vector<float> lo(t.call_ref.size() * TDT_KERNEL_COUNT, 1e30f);
+  std::vector<float> hi(t.call_ref.size() * TDT_KERNEL_COUNT, -1e30f);
   for (auto &pe : t.pending) {
-    float ms = 0.0f;
+    float ms = 0.0f, s0 = 0.0f, s1 = 0.0f;
+    const cudaEvent_t ref = t.call_ref[pe.call];
     if (cudaEventSynchronize(pe.b) != cudaSuccess ||
-        cudaEventElapsedTime(&ms, pe.a, pe.b) != cudaSuccess)
+        cudaEventElapsedTime(&ms, pe.a, pe.b) != cudaSuccess ||
+        cudaEventElapsedTime(&s0, ref, pe.a) != cudaSuccess ||
+        cudaEventElapsedTime(&s1, ref, pe.b) != cudaSuccess)
       rc = TDT_ERR_CUDA;
     t.ms[pe.id] += ms;
     t.count[pe.id] += 1;
+    const size_t k = (size_t)pe.call * TDT_KERNEL_COUNT + pe.id;
+    if (s0 < lo[k]) lo[k] = s0;
+    if (s1 > hi[k]) hi[k] = s1;
     t.pool.push_back(pe.a);
     t.pool.push_back(pe.b);
   }
+  for (size_t k = 0; k < lo.size(); ++k)
+    if (hi[k] >= lo[k]) t.span[k % TDT_KERNEL_COUNT] += hi[k] - lo[k];
   t.pending.clear();
+  for (cudaEvent_t e : t.call_ref) t.pool.push_back(e);
+  t.call_ref.clear();
   if (n > TDT_KERNEL_COUNT) n = TDT_KERNEL_COUNT;
   for (int i = 0; i < n; ++i) {
     if (ms_out) ms_out[i] = t.ms[i];
     if (count_out) count_out[i] = t.count[i];
+    if (span_ms_out) span_ms_out[i] = t.span[i];
   }
   if (reset)
     for (int i = 0; i < TDT_KERNEL_COUNT; ++i) {
       t.ms[i] = 0.0;
+      t.span[i] = 0.0;
       t.count[i] = 0;
     }
   return rc != 0 ? rc : (n < 0 ? 0 : n);

@@ -57,7 +57,6 @@ struct Problem {
   int reduction;
   fx_t sigma_fx;
   long long n_diag;               // T + U1 - 1 anti-diagonals per utterance
-  int rc_stride;                  // floats per row-coefficient record
   int rec_len;                    // fx values per node arc record (arc_record_len)
   int rnnt;                       // 1: plain RNN-T: no duration logits (D = 0); the
                                   //    lattice durations are {0, 1} with blank arcs
@@ -71,17 +70,6 @@ struct Problem {
 // so a lattice pass adds one value per arc; 2D values = a 16-byte multiple.
 __host__ __device__ inline int arc_record_len(int n_dur) { return 2 * n_dur; }
 
-// Row-coefficient record (floats) the gradient pass reads for node n:
-enum RowCoeff {
-  kRcA = 0,      // c_b * N(t,u)   (N = occupancy exp(alpha + beta - logL))
-  kRcLse2 = 1,   // log2 e * log-sum-exp of the token logits
-  kRcLsed2 = 2,  // log2 e * log-sum-exp of the duration logits
-  kRcAB = 3,     // c_b N fB: taken off the blank entry
-  kRcAL = 4,     // c_b N fL: taken off the label entry
-  kRcY = 5,      // label y_{u+1} as int bits (-1: none)
-  kRcLive = 6,   // 1: row inside a usable lattice with N > 0, 0: write zeros
-  kRcD = 8,      // [kRcD + i] = c_b N fD_i
-};
 // Shared memory a K1/K4 block reserves without using it: with it, no K1/K4
 // block fits beside a lattice block (which requests at least
 // kLatticeSmemFloor), so the latency-bound lattice passes get SMs of their own.
@@ -105,7 +93,6 @@ struct Workspace {
   // node-major per-row data, index n = (b * T + t) * U1 + u
   float *lse_tok;  // log-sum-exp of the token logits
   float *lse_dur;  // log-sum-exp of the duration logits
-  float *rowc;     // [nodes][rc_stride] row-coefficient records (RowCoeff)
   float *frac;     // [(2 + D)][nodes]: share of beta(t,u) through blank arcs,
                    //   label arcs, and through each duration
   // per utterance
@@ -232,7 +219,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // ---- host side shared by the entry points (tdt_api.cu) ----------------------
 struct Layout {  // byte offsets of the scratch regions inside one block
-  size_t arcw, alpha, beta, lse_tok, lse_dur, rowc, frac, loglik, scale, usable, total;
+  size_t arcw, alpha, beta, lse_tok, lse_dur, frac, loglik, scale, usable, total;
 };
 bool make_layout(const int64_t sizes[4], int n_dur, Layout *L);
 Workspace carve(const Layout &L, void *base);
@@ -246,15 +233,17 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
 // Rows are flat node ids n in [n_begin, n_end); utterances b in [b_begin, b_end).
 cudaError_t launch_node_tables(const Problem &p, int dtype, const Workspace &ws,
                                long long n_begin, long long n_end, cudaStream_t stream);
+// started (optional): an event recorded once every block of the lattice
+// launch has begun (a launch-completion event); *started_used tells whether
+// it was attached (the plain fallback kernels and launches of more than
+// 65535 utterances do not record it).
 cudaError_t launch_lattice(const Problem &p, const Workspace &ws, long long b_begin,
-                           long long b_end, bool with_beta, cudaStream_t stream);
+                           long long b_end, bool with_beta, cudaStream_t stream,
+                           cudaEvent_t started = nullptr, bool *started_used = nullptr);
 cudaError_t launch_reduce(const Problem &p, const Workspace &ws, float *loss_out,
                           cudaStream_t stream);
 // gscale: device upstream gradient of the loss ([B] for kNone, else [1]) or NULL (= 1)
 cudaError_t launch_grad(const Problem &p, int dtype, const Workspace &ws, void *grad_out,
                         const float *gscale, long long n_begin, long long n_end,
                         cudaStream_t stream);
-cudaError_t launch_row_coeffs(const Problem &p, const Workspace &ws, long long n_begin,
-                              long long n_end, cudaStream_t stream);
-
 }  // namespace tdt

@@ -10,13 +10,15 @@
 // The softmaxes are recomputed from the row and the saved log-sum-exps, so
 // the row is read once more and every gradient element written once, in the
 // input dtype (round to nearest).  Rows outside a lattice are written as 0.
-// A group of TPR threads takes one row (the same grouping as the node-table
-// pass): each thread issues kBatch independent 16-byte loads, then computes
+// A group of TPR threads takes one row (a whole block for rows of 16 KB or
+// more): each thread issues kBatch independent 16-byte loads, then computes
 // and stores them as 16-byte vectors, when the input row and the output row
 // sit at the same offset from a 16-byte boundary (the contiguous case);
-// coalesced scalar accesses otherwise.  The first batch of a row is loaded
-// before the row's coefficient record (written by row_coeff_kernel after the
-// lattice pass), so their latencies overlap.
+// coalesced scalar accesses otherwise.  The row's coefficients (N, fB, fL,
+// fD_i, the saved log-sum-exps, the label) are read from the lattice pass's
+// outputs together with the row's first batch of logits, so their latencies
+// overlap; every lane of a row group computes them (the loads are
+// broadcasts within a warp).
 #include "tdt_rowio.cuh"
 
 namespace tdt {
@@ -24,8 +26,17 @@ namespace tdt {
 namespace {
 
 constexpr int kGradThreads = 256;
-constexpr int kBatch = 8;
-constexpr int kVecPerThread = 8;  // one batch per thread for long rows
+constexpr int kVecPerThread = 8;      // row vectors per lane when choosing TPR
+constexpr int kLongRowBytes = 16384;  // rows from this size on: one block per row
+
+// 16-byte loads a lane issues before it uses them, and the blocks per SM the
+// registers are sized for.  Measured on GB300: 8 loads for one block per row
+// (a long row in one batch) and for 8-lane groups; 4 loads otherwise, which
+// keeps the kernel within 64 registers (four blocks per SM) without spills.
+template <int TPR> struct GradShape {
+  static constexpr int kBatch = (TPR == 256 || TPR == 8) ? 8 : 4;
+  static constexpr int kMinBlocks = TPR == 8 ? 3 : 4;
+};
 
 template <int DT, int TPR>
 __device__ __forceinline__ void zero_row(typename Elem<DT>::T *out, long long VD, int lt) {
@@ -43,12 +54,13 @@ __device__ __forceinline__ void zero_row(typename Elem<DT>::T *out, long long VD
 }
 
 template <int DT, int TPR, bool COH>
-__global__ void __launch_bounds__(kGradThreads, TPR == 256 ? 4 : 3)
+__global__ void __launch_bounds__(kGradThreads, GradShape<TPR>::kMinBlocks)
 grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gscale,
             long long n_begin, long long n_end) {
   typedef typename Elem<DT>::T E;
   constexpr int N = Vec<DT>::N;
   constexpr int RPB = kGradThreads / TPR;
+  constexpr int kBatch = GradShape<TPR>::kBatch;
   constexpr int kDurPerLane = (kMaxDurations + TPR - 1) / TPR;  // D <= kMaxDurations
   const E *logits = static_cast<const E *>(p.logits);
   const int lt = threadIdx.x % TPR;
@@ -62,8 +74,9 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
   const bool in_lattice = t < Tb && u <= Ub;
   // Everything the row needs is loaded up front, so its latencies overlap:
   // the first batch of 16-byte vectors, the scalar head and tail, the
-  // duration logits and their coefficients (lane lt: durations lt, lt + TPR,
-  // ...), the row's coefficient record and the upstream gradient.
+  // duration logits and their fractions (lane lt: durations lt, lt + TPR,
+  // ...), alpha, beta and the other lattice outputs of the row, and the
+  // upstream gradient.
   const uintptr_t ai = reinterpret_cast<uintptr_t>(row), ao = reinterpret_cast<uintptr_t>(out);
   const bool vec = ((ai ^ ao) & 15) == 0;
   int head = head_elems<DT>(row);
@@ -72,9 +85,14 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
   const long long tail0 = head + (long long)nvec * N;
   const int ntail = (int)(p.V - tail0);
   const uint4 *vin = reinterpret_cast<const uint4 *>(row + head);
-  const float *rc = ws.rowc + n * p.rc_stride;
+  const long long nodes = p.B * p.T * p.U1;
   uint4 v[kBatch];
-  float zh = 0.0f, zt = 0.0f, zd[kDurPerLane], rcd[kDurPerLane];
+  float zh = 0.0f, zt = 0.0f, zd[kDurPerLane], fd[kDurPerLane];
+  LV al = {}, be = {}, ll = {};
+  double sc = 0.0;
+  int usable = 0;
+  float lse_t = 0.0f, lse_d = 0.0f, fb = 0.0f, fl = 0.0f;
+  long long y = -1;
   if (in_lattice) {
     if (vec) {
 #pragma unroll
@@ -89,23 +107,36 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
     for (int c = 0; c < kDurPerLane; ++c) {
       const int i = lt + c * TPR;
       zd[c] = i < p.D ? ld_elem<DT, COH>(row + p.V + i) : 0.0f;
-      rcd[c] = i < p.D ? rc[kRcD + i] : 0.0f;
+      fd[c] = i < p.D ? ws.frac[(long long)(2 + i) * nodes + n] : 0.0f;
     }
+    const long long q = diag_index(p, b, t, u);
+    al = ws.alpha[q];
+    be = ws.beta[q];
+    ll = ws.loglik[b];
+    sc = ws.scale[b];
+    usable = ws.usable[b];
+    lse_t = ws.lse_tok[n];
+    lse_d = ws.lse_dur[n];
+    fb = ws.frac[n];
+    fl = ws.frac[nodes + n];
+    if (u < Ub) y = p.labels[b * (p.U1 - 1) + u];
   }
   // upstream gradient of utterance b's loss (1 when none is given; x * 1 is exact)
   const float gs = gscale ? gscale[p.reduction == kNone ? b : 0] : 1.0f;
-  const float4 r0 = *reinterpret_cast<const float4 *>(rc);
-  const float4 r1 = *reinterpret_cast<const float4 *>(rc + 4);
-  if (!in_lattice || r1.z == 0.0f) {
+  // rows outside a usable lattice, or of zero occupancy, get a zero gradient
+  if (!in_lattice || !usable || al.s == 0.0f || be.s == 0.0f || ll.s == 0.0f) {
     zero_row<DT, TPR>(out, p.VD, lt);
     return;
   }
-  const float a = r0.x * gs, lse2 = r0.y, lsed2 = r0.z, ab = r0.w * gs, al = r1.x * gs;
-  const int y = __float_as_int(r1.y);
+  // c_b N with N = exp(alpha + beta - logL) = 2^((m_a + m_b - m_L) log2 e) s_a s_b / s_L
+  const float a0 =
+      (float)sc * (fast_exp2(__ll2float_rn(al.m + be.m - ll.m) * kFxToLog2) * (al.s * be.s / ll.s));
+  const float a = a0 * gs, lse2 = lse_t * kLog2e, lsed2 = lse_d * kLog2e;
+  const float ab = (a0 * fb) * gs, alb = (a0 * fl) * gs;
   auto g_at = [&](float x, long long k) {
     float g = a * fast_exp2(fmaf(x, kLog2e, -lse2));
     if (k == p.blank) g -= ab;
-    if (k == y) g -= al;
+    if (k == y) g -= alb;
     return g;
   };
 
@@ -134,7 +165,7 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
 #pragma unroll
           for (int e = 0; e < N; ++e) x[e] = a * fast_exp2(fmaf(x[e], kLog2e, -lse2));
           if (j == jb) x[eb] -= ab;
-          if (j == jy) x[ey] -= al;
+          if (j == jy) x[ey] -= alb;
           vout[j] = pack<DT>(x);
         }
       }
@@ -159,51 +190,8 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
     const int i = lt + c * TPR;
     if (i < p.D)
       out[p.V + i] =
-          Elem<DT>::from_float(a * fast_exp2(fmaf(zd[c], kLog2e, -lsed2)) - rcd[c] * gs);
+          Elem<DT>::from_float(a * fast_exp2(fmaf(zd[c], kLog2e, -lsed2)) - (a0 * fd[c]) * gs);
   }
-}
-
-// Row-coefficient records for rows [n_begin, n_end): everything the gradient
-// pass needs about a node besides its logits row, in one record per row.
-__global__ void row_coeff_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) {
-  const long long n = n_begin + (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (n >= n_end) return;
-  const long long nodes = p.B * p.T * p.U1;
-  long long b, t, u;
-  decode_node(p, n, &b, &t, &u);
-  float *rc = ws.rowc + n * p.rc_stride;
-  const long long Tb = p.logit_lens[b], Ub = p.label_lens[b];
-  bool live = ws.usable[b] && t < Tb && u <= Ub;
-  float a = 0.0f;
-  if (live) {
-    // N = exp(alpha + beta - logL) = 2^((m_a + m_b - m_L) log2 e) * s_a * s_b / s_L
-    const long long q = diag_index(p, b, t, u);
-    const LV al = ws.alpha[q], be = ws.beta[q], ll = ws.loglik[b];
-    if (al.s == 0.0f || be.s == 0.0f || ll.s == 0.0f) {
-      live = false;
-    } else {
-      const fx_t dm = al.m + be.m - ll.m;
-      const float occ = fast_exp2(__ll2float_rn(dm) * kFxToLog2) * (al.s * be.s / ll.s);
-      a = (float)ws.scale[b] * occ;
-    }
-  }
-  if (!live) {
-    rc[kRcLive] = 0.0f;
-    return;
-  }
-  const int y = (u < Ub) ? (int)p.labels[b * (p.U1 - 1) + u] : -1;
-  float4 r0, r1;
-  r0.x = a;
-  r0.y = ws.lse_tok[n] * kLog2e;
-  r0.z = ws.lse_dur[n] * kLog2e;
-  r0.w = a * ws.frac[n];
-  r1.x = a * ws.frac[nodes + n];
-  r1.y = __int_as_float(y);
-  r1.z = 1.0f;
-  r1.w = 0.0f;
-  *reinterpret_cast<float4 *>(rc) = r0;
-  *reinterpret_cast<float4 *>(rc + 4) = r1;
-  for (int i = 0; i < p.D; ++i) rc[kRcD + i] = a * ws.frac[(long long)(2 + i) * nodes + n];
 }
 
 template <int DT, int TPR>
@@ -219,12 +207,9 @@ cudaError_t launch_tpr(const Problem &p, const Workspace &ws, typename Elem<DT>:
   const long long span = (p.B - 1) * p.s0 + (p.T - 1) * p.s1 + (p.U1 - 1) * p.s2 + p.VD;
   const bool overlap = p.B > 0 && go < lo + span * (long long)sizeof(*grad) &&
                        lo < go + p.B * p.T * p.U1 * p.VD * (long long)sizeof(*grad);
-  if (overlap)
-    grad_kernel<DT, TPR, true><<<(unsigned)blocks, kGradThreads, kStreamSmemReserve, stream>>>(
-        p, ws, grad, gscale, n_begin, n_end);
-  else
-    grad_kernel<DT, TPR, false><<<(unsigned)blocks, kGradThreads, kStreamSmemReserve, stream>>>(
-        p, ws, grad, gscale, n_begin, n_end);
+  auto kern = overlap ? grad_kernel<DT, TPR, true> : grad_kernel<DT, TPR, false>;
+  kern<<<(unsigned)blocks, kGradThreads, kStreamSmemReserve, stream>>>(p, ws, grad, gscale,
+                                                                       n_begin, n_end);
   return cudaGetLastError();
 }
 
@@ -233,7 +218,9 @@ cudaError_t launch_dt(const Problem &p, const Workspace &ws, void *grad_out, con
                       long long n_begin, long long n_end, cudaStream_t stream) {
   typedef typename Elem<DT>::T E;
   E *g = static_cast<E *>(grad_out);
-  const int tpr = row_group_threads(p.V * (long long)sizeof(E), kVecPerThread);
+  const long long row_bytes = p.V * (long long)sizeof(E);
+  const int tpr =
+      row_bytes >= kLongRowBytes ? 256 : row_group_threads(row_bytes, kVecPerThread);
   switch (tpr) {
     case 8: return launch_tpr<DT, 8>(p, ws, g, gscale, n_begin, n_end, stream);
     case 16: return launch_tpr<DT, 16>(p, ws, g, gscale, n_begin, n_end, stream);
@@ -245,14 +232,6 @@ cudaError_t launch_dt(const Problem &p, const Workspace &ws, void *grad_out, con
 }
 
 }  // namespace
-
-cudaError_t launch_row_coeffs(const Problem &p, const Workspace &ws, long long n_begin,
-                              long long n_end, cudaStream_t stream) {
-  const long long rows = n_end - n_begin;
-  if (rows <= 0) return cudaSuccess;
-  row_coeff_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(p, ws, n_begin, n_end);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_grad(const Problem &p, int dtype, const Workspace &ws, void *grad_out,
                         const float *gscale, long long n_begin, long long n_end,

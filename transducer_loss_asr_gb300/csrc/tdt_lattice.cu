@@ -774,7 +774,7 @@ int preferred_bands(const Problem &p) {
 template <int ND, int G>
 cudaError_t launch_cluster_g(const Problem &p, const Workspace &ws, long long b0, long long nb,
                              bool with_beta, const ClusterPlan &cp, cudaStream_t stream,
-                             bool *placed) {
+                             bool *placed, cudaEvent_t started, bool *started_used) {
   *placed = false;
   auto kern = cp.K > 1 ? lattice_cluster_kernel<ND, G, true, kPrefetch>
                        : (cp.P == kPrefetchDeep ? lattice_cluster_kernel<ND, G, false, kPrefetchDeep>
@@ -787,24 +787,34 @@ cudaError_t launch_cluster_g(const Problem &p, const Workspace &ws, long long b0
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   const dim3 grid((unsigned)cp.K, (unsigned)nb, with_beta ? 2u : 1u);
-  if (cp.K == 1) {
-    // one band: an ordinary launch (a CTA outside a cluster is a cluster of one)
-    *placed = true;
-    kern<<<grid, cp.threads, bytes, stream>>>(p, ws, b0, cp);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3((unsigned)cp.threads, 1, 1);
   cfg.dynamicSmemBytes = bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)cp.K;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (started) {
+    attr[na].id = cudaLaunchAttributeLaunchCompletionEvent;
+    attr[na].val.launchCompletionEvent.event = started;
+    attr[na].val.launchCompletionEvent.flags = 0;
+    ++na;
+  }
+  if (cp.K == 1) {
+    // one band: an ordinary launch (a CTA outside a cluster is a cluster of one)
+    *placed = true;
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    if (started_used) *started_used = started != nullptr;
+    return cudaLaunchKernelEx(&cfg, kern, p, ws, b0, cp);
+  }
+  attr[na].id = cudaLaunchAttributeClusterDimension;
+  attr[na].val.clusterDim.x = (unsigned)cp.K;
+  attr[na].val.clusterDim.y = 1;
+  attr[na].val.clusterDim.z = 1;
+  ++na;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = na;
   // a cluster of K CTAs of this size must fit the GPU at all (asked once per
   // device and shape)
   int dev = 0;
@@ -827,31 +837,51 @@ cudaError_t launch_cluster_g(const Problem &p, const Workspace &ws, long long b0
   }
   *placed = clusters >= 1;
   if (!*placed) return cudaSuccess;
+  if (started_used) *started_used = started != nullptr;
   return cudaLaunchKernelEx(&cfg, kern, p, ws, b0, cp);
 }
 
 template <int ND>
 cudaError_t launch_cluster(const Problem &p, const Workspace &ws, long long b0, long long nb,
                            bool with_beta, const ClusterPlan &cp, cudaStream_t stream,
-                           bool *placed) {
-  return launch_cluster_g<ND, group_lanes(ND)>(p, ws, b0, nb, with_beta, cp, stream, placed);
+                           bool *placed, cudaEvent_t started, bool *started_used) {
+  return launch_cluster_g<ND, group_lanes(ND)>(p, ws, b0, nb, with_beta, cp, stream, placed,
+                                               started, started_used);
 }
 
 // Launch the cluster variant; *placed is false (nothing launched) when a
 // cluster of cp.K CTAs of this size does not fit the GPU.
 cudaError_t launch_cluster_nd(const Problem &p, const Workspace &ws, long long b0, long long nb,
                               bool with_beta, const ClusterPlan &cp, cudaStream_t stream,
-                              bool *placed) {
+                              bool *placed, cudaEvent_t started, bool *started_used) {
   switch (p.n_dur) {
-    case 1: return launch_cluster<1>(p, ws, b0, nb, with_beta, cp, stream, placed);
-    case 2: return launch_cluster<2>(p, ws, b0, nb, with_beta, cp, stream, placed);
-    case 3: return launch_cluster<3>(p, ws, b0, nb, with_beta, cp, stream, placed);
-    case 4: return launch_cluster<4>(p, ws, b0, nb, with_beta, cp, stream, placed);
-    case 5: return launch_cluster<5>(p, ws, b0, nb, with_beta, cp, stream, placed);
-    case 6: return launch_cluster<6>(p, ws, b0, nb, with_beta, cp, stream, placed);
-    case 7: return launch_cluster<7>(p, ws, b0, nb, with_beta, cp, stream, placed);
-    case 8: return launch_cluster<8>(p, ws, b0, nb, with_beta, cp, stream, placed);
-    default: return launch_cluster<9>(p, ws, b0, nb, with_beta, cp, stream, placed);
+    case 1:
+      return launch_cluster<1>(p, ws, b0, nb, with_beta, cp, stream, placed, started,
+                                started_used);
+    case 2:
+      return launch_cluster<2>(p, ws, b0, nb, with_beta, cp, stream, placed, started,
+                                started_used);
+    case 3:
+      return launch_cluster<3>(p, ws, b0, nb, with_beta, cp, stream, placed, started,
+                                started_used);
+    case 4:
+      return launch_cluster<4>(p, ws, b0, nb, with_beta, cp, stream, placed, started,
+                                started_used);
+    case 5:
+      return launch_cluster<5>(p, ws, b0, nb, with_beta, cp, stream, placed, started,
+                                started_used);
+    case 6:
+      return launch_cluster<6>(p, ws, b0, nb, with_beta, cp, stream, placed, started,
+                                started_used);
+    case 7:
+      return launch_cluster<7>(p, ws, b0, nb, with_beta, cp, stream, placed, started,
+                                started_used);
+    case 8:
+      return launch_cluster<8>(p, ws, b0, nb, with_beta, cp, stream, placed, started,
+                                started_used);
+    default:
+      return launch_cluster<9>(p, ws, b0, nb, with_beta, cp, stream, placed, started,
+                                started_used);
   }
 }
 
@@ -898,7 +928,10 @@ __global__ void reduce_kernel(Problem p, Workspace ws, float *loss_out) {
 
 
 cudaError_t launch_lattice(const Problem &p, const Workspace &ws, long long b_begin,
-                           long long b_end, bool with_beta, cudaStream_t stream) {
+                           long long b_end, bool with_beta, cudaStream_t stream,
+                           cudaEvent_t started, bool *started_used) {
+  if (started_used) *started_used = false;
+  if (b_end - b_begin > 65535) started = nullptr;
   // grid.y is at most 65535: launch in groups of utterances
   for (long long g0 = b_begin; g0 < b_end; g0 += 65535) {
     const long long nb = (b_end - g0 < 65535) ? b_end - g0 : 65535;
@@ -913,7 +946,8 @@ cudaError_t launch_lattice(const Problem &p, const Workspace &ws, long long b_be
       ClusterPlan cp;
       if (!cluster_plan(p, K, &cp)) continue;
       bool placed = false;
-      const cudaError_t e = launch_cluster_nd(p, ws, g0, nb, with_beta, cp, stream, &placed);
+      const cudaError_t e =
+          launch_cluster_nd(p, ws, g0, nb, with_beta, cp, stream, &placed, started, started_used);
       if (e != cudaSuccess) return e;
       done = placed;
     }

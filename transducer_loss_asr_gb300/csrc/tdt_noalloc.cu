@@ -81,7 +81,6 @@ extern "C" int tdt_loss_fwd_bwd_noalloc(const void *logits, const int64_t sizes[
   const bool with_grad = grad_out != nullptr;
   if (tdt::launch_node_tables(p, dtype, ws, 0, rows, s) != cudaSuccess) return TDT_ERR_CUDA;
   if (tdt::launch_lattice(p, ws, 0, p.B, with_grad, s) != cudaSuccess) return TDT_ERR_CUDA;
-  if (with_grad && tdt::launch_row_coeffs(p, ws, 0, rows, s) != cudaSuccess) return TDT_ERR_CUDA;
   if (tdt::launch_reduce(p, ws, loss_out, s) != cudaSuccess) return TDT_ERR_CUDA;
   if (with_grad && tdt::launch_grad(p, dtype, ws, grad_out, nullptr, 0, rows, s) != cudaSuccess)
     return TDT_ERR_CUDA;

@@ -107,10 +107,12 @@ template <int DT> __device__ __forceinline__ int head_elems(const void *p) {
 namespace tdt {
 
 // Threads per row group for a row of row_bytes: the smallest power of two in
-// [8, 256] that covers the row with `batch` 16-byte loads per thread.
+// [8, 256] whose `batch` 16-byte loads per thread cover the row's vector
+// body.  The body holds at most row_bytes / 16 whole vectors (the head and
+// tail around it are scalar accesses).
 inline int row_group_threads(long long row_bytes, int batch) {
   int t = 8;
-  while (t < 256 && (long long)t * batch * 16 < row_bytes) t <<= 1;
+  while (t < 256 && (long long)t * batch < row_bytes / 16) t <<= 1;
   return t;
 }
 
