@@ -8,7 +8,11 @@ gradient) over one batch of the workload, inputs already in HBM.  L2 is
 flushed (a 2x-L2 buffer is written) between timed steps, outside the events.
 Prints one JSON line (rank 0).  ``value`` is achieved HBM throughput over the
 algorithmic bytes of the step (valid-node logits read once + every gradient
-element written once); ``ms_per_step`` the time of one step.
+element written once); ``ms_per_step`` the time of one step.  The steps are
+timed twice: once as a user runs them (``value``, ``ms_per_step``), then
+again with the library's per-kernel CUDA events for the per-kernel times, the
+roofline of the gradient pass and the launch count (those events sit between
+the kernels on their streams and lengthen the step by a few percent).
 
 Under torchrun (N > 1) every rank runs its own replica of the workload (the
 loss shards by utterance; there is no exchange on the path): weak scaling,
@@ -46,11 +50,11 @@ FALLBACK_HBM_GBS = 6800.0
 # its sources hash to this sha256 (kernel_sha).
 NCU_TRAFFIC = {
     # ncu --set full, one launch = one utterance [1,200,41,8198] fp32 (the
-    # per-launch work of the four-chunk B=4 bench): read 269653504 + written
-    # 209491200 bytes (the rest of the writes retire from L2 after the kernel)
+    # per-launch work of the four-chunk B=4 bench): read 269838336 + written
+    # 209677824 bytes (the rest of the writes retire from L2 after the kernel)
     ("grad", "parakeet"): {
-        "bytes": 269653504 + 209491200,
-        "sha256": "fc9d7001b6169a363f3fe16da88c8090bc5d477bbfe382bfc95f218666b5db60",
+        "bytes": 269838336 + 209677824,
+        "sha256": "4cb469a475b198202643b7a4e7e28ca180de0924712b327609ed9921f45b6fe1",
     },
 }
 
@@ -382,29 +386,42 @@ def main():
         step()
     torch.cuda.synchronize()
 
+    def timed_steps(kernel_events):
+        """K steps, L2 flushed before each (outside the events), CUDA events
+        around each step on the launching stream; returns the summed ms.
+        With kernel_events the library also records events around each of
+        its kernels (on the stream each runs on) -- they sit between the
+        kernels on the streams and lengthen the step, so the headline step
+        time comes from a run without them."""
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        binding.tdt_loss_timing_read(reset=True)
+        binding.tdt_loss_timing_enable(kernel_events)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(i & 0xff)
+            starts[i].record()
+            step()
+            ends[i].record()
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        binding.tdt_loss_timing_enable(False)
+        return sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+
+    # headline: the steps as a user runs them (no per-kernel events)
     sampler = ClockSampler(local) if local == 0 else None
-    binding.tdt_loss_timing_read(reset=True)
-    binding.tdt_loss_timing_enable(True)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
     if sampler:
         sampler.start()
-    for i in range(args.steps):
-        flush.fill_(i & 0xff)
-        starts[i].record()
-        step()
-        ends[i].record()
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
+    total_ms = timed_steps(False)
     if sampler:
         sampler.stop()
-    binding.tdt_loss_timing_enable(False)
+    # per-kernel breakdown, roofline and launch count: the same steps again
+    # with the library's per-kernel events
+    kernel_step_ms = timed_steps(True) / args.steps
     kt = binding.tdt_loss_timing_read(reset=True)
-    total_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
     t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if dist is not None:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -516,6 +533,9 @@ def main():
             "algorithmic_bytes_per_step": step_bytes,
             "roofline": roofline,
             "kernels": per_kernel,
+            "kernel_timing": ("a second timed run of the same steps with per-kernel CUDA events "
+                              "(its step: %.4f ms); value and ms_per_step come from the run "
+                              "without them" % kernel_step_ms),
             "gpu_launches": int(sum(v[1] for v in kt.values())),
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,

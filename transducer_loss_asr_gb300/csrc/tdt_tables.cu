@@ -55,7 +55,7 @@ __device__ __forceinline__ void group_ms(float &m, float &s, float *sm_m, float 
     const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
     merge_ms(m, s, m2, s2);
   }
-  if (TPR > 32) {
+  if constexpr (TPR > 32) {
     constexpr int NW = TPR / 32;  // warps per group
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) {
