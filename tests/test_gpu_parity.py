@@ -97,6 +97,17 @@ MEDIUM = {
                              T_range=(10, 29), U_range=(1, 9), base_vd=790),
     "f16_full": dict(B=2, T=18, U=6, V=513, blank=512, durations=(0, 1, 2), dtype="f16",
                      std=1.0, sigma=0.0, reduction="sum"),
+    # strided views whose rows sit at varying offsets from the gradient rows'
+    # 16-byte boundaries (the realigned vector path), short and long rows
+    "f16_ragged_view": dict(B=3, T=21, U=7, V=555, blank=554, durations=(0, 1, 2, 3, 4),
+                            dtype="f16", std=1.0, sigma=0.05, reduction="mean_volume",
+                            T_range=(9, 21), U_range=(2, 7), base_vd=571),
+    "bf16_short_view": dict(B=3, T=17, U=5, V=45, blank=44, durations=(0, 1, 2),
+                            dtype="bf16", std=1.0, sigma=0.0, reduction="sum",
+                            T_range=(8, 17), U_range=(1, 5), base_vd=61),
+    "f32_short_view": dict(B=2, T=13, U=4, V=37, blank=36, durations=(0, 2, 3), dtype="f32",
+                           std=1.0, sigma=0.02, reduction="mean_batch", T_range=(6, 13),
+                           U_range=(1, 4), base_vd=50),
     "f32_no_zero_duration": dict(B=2, T=25, U=5, V=64, blank=63, durations=(1, 2, 4),
                                  dtype="f32", std=2.0, sigma=0.02, reduction="none",
                                  T_range=(12, 25), U_range=(0, 5)),

@@ -14,7 +14,8 @@
 // more): each thread issues kBatch independent 16-byte loads, then computes
 // and stores them as 16-byte vectors, when the input row and the output row
 // sit at the same offset from a 16-byte boundary (the contiguous case);
-// coalesced scalar accesses otherwise.  The row's coefficients (N, fB, fL,
+// otherwise (a strided view) output-aligned 16-byte vectors assembled from
+// the two aligned input vectors each one spans.  The row's coefficients (N, fB, fL,
 // fD_i, the saved log-sum-exps, the label) are read from the lattice pass's
 // outputs together with the row's first batch of logits, so their latencies
 // overlap; every lane of a row group computes them (the loads are
@@ -53,7 +54,10 @@ __device__ __forceinline__ void zero_row(typename Elem<DT>::T *out, long long VD
   for (int j = lt; j < nvec; j += TPR) v[j] = make_uint4(0u, 0u, 0u, 0u);
 }
 
-template <int DT, int TPR, bool COH>
+// VIEW: the logits rows may sit at another offset from a 16-byte boundary
+// than the gradient rows (a strided view); without it every row is known to
+// share the gradient row's alignment (one contiguous layout).
+template <int DT, int TPR, bool COH, bool VIEW>
 __global__ void __launch_bounds__(kGradThreads, GradShape<TPR>::kMinBlocks)
 grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gscale,
             long long n_begin, long long n_end) {
@@ -78,7 +82,8 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
   // ...), alpha, beta and the other lattice outputs of the row, and the
   // upstream gradient.
   const uintptr_t ai = reinterpret_cast<uintptr_t>(row), ao = reinterpret_cast<uintptr_t>(out);
-  const bool vec = ((ai ^ ao) & 15) == 0;
+  // without VIEW the host has checked that every row shares the output's alignment
+  const bool vec = !VIEW || ((ai ^ ao) & 15) == 0;
   int head = head_elems<DT>(row);
   if (head > p.V) head = (int)p.V;
   const int nvec = (int)((p.V - head) / N);
@@ -170,18 +175,63 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
         }
       }
     }
-  } else {
-    for (long long k0 = 0; k0 < p.V; k0 += TPR * kBatch) {
-      float x[kBatch];
+  } else if constexpr (VIEW) {
+    // The input and output rows sit at different offsets from a 16-byte
+    // boundary (a strided view of a wider tensor): output-aligned 16-byte
+    // vectors, each assembled from the two aligned input vectors it spans
+    // (the second is the next lane's first, served by L1).  Vectors whose
+    // input span would leave the row, and the output's scalar head and
+    // tail, take element accesses.
+    int oh = head_elems<DT>(out);
+    if (oh > p.V) oh = (int)p.V;
+    const int onv = (int)((p.V - oh) / N);
+    const long long ot0 = oh + (long long)onv * N;
+    const uintptr_t rlo = reinterpret_cast<uintptr_t>(row);
+    const uintptr_t rhi = rlo + (uintptr_t)p.V * sizeof(E);
+    const uintptr_t first = reinterpret_cast<uintptr_t>(row + oh);
+    const int sh = (int)(first & 15);  // the same for every output vector
+    const int qw = sh >> 2, rb = (sh & 3) * 8;
+    const uintptr_t abase = first - (uintptr_t)sh;
+    const uintptr_t span = sh ? 32 : 16;
+    if (lt < oh) out[lt] = Elem<DT>::from_float(g_at(ld_elem<DT, COH>(row + lt), lt));
+    if (lt < p.V - ot0)
+      out[ot0 + lt] = Elem<DT>::from_float(g_at(ld_elem<DT, COH>(row + ot0 + lt), ot0 + lt));
+    uint4 *vout = reinterpret_cast<uint4 *>(out + oh);
+    const int jb = (p.blank >= oh && p.blank < ot0) ? (int)((p.blank - oh) / N) : -1;
+    const int jy = (y >= oh && y < ot0) ? (int)((y - oh) / N) : -1;
+    const int eb = (int)((p.blank - oh) % N), ey = (int)((y - oh) % N);
+    // half the batch: two vectors per output vector in flight
+    constexpr int kFB = kBatch / 2;
+    for (int j0 = 0; j0 < onv; j0 += TPR * kFB) {
+      uint4 lo[kFB], hi[kFB];
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const long long k = k0 + i * TPR + lt;
-        x[i] = (k < p.V) ? ld_elem<DT, COH>(row + k) : 0.0f;
+      for (int i = 0; i < kFB; ++i) {
+        const int j = j0 + i * TPR + lt;
+        const uintptr_t A = abase + 16 * (uintptr_t)j;
+        if (j < onv && A >= rlo && A + span <= rhi) {
+          lo[i] = ld_row16_l1<COH>(reinterpret_cast<const void *>(A));
+          hi[i] = sh ? ld_row16_l1<COH>(reinterpret_cast<const void *>(A + 16)) : lo[i];
+        }
       }
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const long long k = k0 + i * TPR + lt;
-        if (k < p.V) out[k] = Elem<DT>::from_float(g_at(x[i], k));
+      for (int i = 0; i < kFB; ++i) {
+        const int j = j0 + i * TPR + lt;
+        if (j < onv) {
+          const uintptr_t A = abase + 16 * (uintptr_t)j;
+          const long long k0 = oh + (long long)N * j;
+          float x[N];
+          if (A >= rlo && A + span <= rhi) {
+            unpack<DT>(funnel16(lo[i], hi[i], qw, rb), x);
+          } else {
+#pragma unroll
+            for (int e = 0; e < N; ++e) x[e] = ld_elem<DT, COH>(row + k0 + e);
+          }
+#pragma unroll
+          for (int e = 0; e < N; ++e) x[e] = a * fast_exp2(fmaf(x[e], kLog2e, -lse2));
+          if (j == jb) x[eb] -= ab;
+          if (j == jy) x[ey] -= alb;
+          vout[j] = pack<DT>(x);
+        }
       }
     }
   }
@@ -207,7 +257,16 @@ cudaError_t launch_tpr(const Problem &p, const Workspace &ws, typename Elem<DT>:
   const long long span = (p.B - 1) * p.s0 + (p.T - 1) * p.s1 + (p.U1 - 1) * p.s2 + p.VD;
   const bool overlap = p.B > 0 && go < lo + span * (long long)sizeof(*grad) &&
                        lo < go + p.B * p.T * p.U1 * p.VD * (long long)sizeof(*grad);
-  auto kern = overlap ? grad_kernel<DT, TPR, true> : grad_kernel<DT, TPR, false>;
+  // one layout for logits and gradient, at the same offset from a 16-byte
+  // boundary: every row takes the aligned vector path
+  const bool same_layout = p.s2 == p.VD && p.s1 == p.U1 * p.VD && p.s0 == p.T * p.s1 &&
+                           ((reinterpret_cast<uintptr_t>(lo) - reinterpret_cast<uintptr_t>(go)) &
+                            15) == 0;
+  // (an output that overlaps the logits is the contiguous logits themselves:
+  // the argument checks reject any other overlap)
+  auto kern = overlap       ? grad_kernel<DT, TPR, true, false>
+              : same_layout ? grad_kernel<DT, TPR, false, false>
+                            : grad_kernel<DT, TPR, false, true>;
   kern<<<(unsigned)blocks, kGradThreads, kStreamSmemReserve, stream>>>(p, ws, grad, gscale,
                                                                        n_begin, n_end);
   return cudaGetLastError();

@@ -34,6 +34,37 @@ template <bool COH> __device__ __forceinline__ uint4 ld_row16(const uint4 *p) {
   return v;
 }
 
+// 16-byte load that allocates in L1: for vectors that neighbouring lanes
+// read twice (the realigned gradient path).  Read-only path unless COH.
+template <bool COH> __device__ __forceinline__ uint4 ld_row16_l1(const void *p) {
+  uint4 v;
+  if (COH)
+    asm volatile("ld.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+  else
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+  return v;
+}
+
+// The 16 bytes that start `qw` words plus `rb` bits into the 32-byte pair
+// (lo, hi), qw in [0, 3], rb in {0, 8, 16, 24}.
+__device__ __forceinline__ uint4 funnel16(uint4 lo, uint4 hi, int qw, int rb) {
+  // shift by whole words: 2 then 1
+  unsigned w0 = lo.x, w1 = lo.y, w2 = lo.z, w3 = lo.w, w4 = hi.x, w5 = hi.y, w6 = hi.z,
+           w7 = hi.w;
+  if (qw & 2) {
+    w0 = w2; w1 = w3; w2 = w4; w3 = w5; w4 = w6; w5 = w7;
+  }
+  if (qw & 1) {
+    w0 = w1; w1 = w2; w2 = w3; w3 = w4; w4 = w5;
+  }
+  return make_uint4(__funnelshift_r(w0, w1, rb), __funnelshift_r(w1, w2, rb),
+                    __funnelshift_r(w2, w3, rb), __funnelshift_r(w3, w4, rb));
+}
+
 // One element as float, read-only path unless COH.
 template <int DT, bool COH>
 __device__ __forceinline__ float ld_elem(const typename Elem<DT>::T *p) {
