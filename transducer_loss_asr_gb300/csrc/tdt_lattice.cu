@@ -765,10 +765,23 @@ bool cluster_plan(const Problem &p, int K, ClusterPlan *cp) {
   return false;
 }
 
-int preferred_bands(const Problem &p) {
+// Bands per utterance and direction for a launch of nb utterances.  A
+// diagonal step is bound by issuing the work of all of a CTA's warps, so an
+// utterance whose single band would hold more than 16 warps is split into
+// bands of about 12 warps (measured on large_batch, 121 rows: one band of 31
+// warps 1.16 us per diagonal, three bands of 11 warps 0.93 us with the
+// exchange); parakeet's 11-warp band stays whole (two bands: 40% slower).
+// The bands of a launch take an SM each, so a launch holds at most ~48 of
+// them; the rest of the GPU streams K1/K4.
+int preferred_bands(const Problem &p, long long nb) {
   const int forced = g_forced_bands.load();
   if (forced > 0) return forced < kMaxCluster ? forced : kMaxCluster;
-  return 1;
+  const int warps = (int)(((p.U1 + 1) * group_lanes(p.n_dur) + 31) / 32);
+  if (warps <= 16) return 1;
+  int K = (warps + 11) / 12;
+  const long long cap = 48 / (2 * (nb > 0 ? nb : 1));
+  if (K > cap) K = cap > 1 ? (int)cap : 1;
+  return K < kMaxCluster ? K : kMaxCluster;
 }
 
 template <int ND, int G>
@@ -939,7 +952,7 @@ cudaError_t launch_lattice(const Problem &p, const Workspace &ws, long long b_be
     // K bands per utterance: the preferred count, else more bands (fewer
     // rows, when a band needs too many threads or too much shared memory),
     // else fewer (when a cluster of K CTAs does not fit the GPU)
-    const int K0 = preferred_bands(p);
+    const int K0 = preferred_bands(p, nb);
     for (int step = 0; step < 2 * kMaxCluster && !done; ++step) {
       const int K = step < kMaxCluster - K0 + 1 ? K0 + step : K0 - (step - (kMaxCluster - K0));
       if (K < 1 || K > kMaxCluster) continue;
