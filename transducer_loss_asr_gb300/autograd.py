@@ -45,7 +45,7 @@ def workspace_nbytes(B, T, U1, n_dur):
     nodes = B * T * U1
     rec_len = 2 * n_dur
     regions = (ndiag * 8 * rec_len, ndiag * 16, ndiag * 16, nodes * 4, nodes * 4,
-               nodes * 4 * (2 + n_dur), B * 16, B * 8, B * 4)
+               nodes * 4 * (2 + n_dur), B * 16, B * 4, B * 4)
     off = 0
     for r in regions:
         off = _align(off + r)

@@ -58,7 +58,7 @@ bool make_layout(const int64_t sizes[4], int n_dur, Layout *L) {
   L->lse_dur = take(nodes * 4);
   L->frac = take(nodes * 4 * (size_t)(2 + n_dur));
   L->loglik = take((size_t)B * sizeof(LV));
-  L->scale = take((size_t)B * 8);
+  L->scale = take((size_t)B * 4);
   L->usable = take((size_t)B * 4);
   L->total = off > 0 ? off : 256;
   return true;
@@ -74,7 +74,7 @@ Workspace carve(const Layout &L, void *base) {
   w.lse_dur = reinterpret_cast<float *>(c + L.lse_dur);
   w.frac = reinterpret_cast<float *>(c + L.frac);
   w.loglik = reinterpret_cast<LV *>(c + L.loglik);
-  w.scale = reinterpret_cast<double *>(c + L.scale);
+  w.scale = reinterpret_cast<float *>(c + L.scale);
   w.usable = reinterpret_cast<int *>(c + L.usable);
   return w;
 }

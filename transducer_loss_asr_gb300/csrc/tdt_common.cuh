@@ -97,7 +97,7 @@ struct Workspace {
                    //   label arcs, and through each duration
   // per utterance
   LV *loglik;      // [B] log-likelihood from alpha (s = 0: no path)
-  double *scale;   // [B] c_b, factor of dL_b/dz in the reduced loss
+  float *scale;    // [B] c_b, factor of dL_b/dz in the reduced loss
   int *usable;     // [B] 1 = lengths and labels usable
 };
 

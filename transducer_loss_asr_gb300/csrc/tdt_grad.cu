@@ -94,7 +94,7 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
   uint4 v[kBatch];
   float zh = 0.0f, zt = 0.0f, zd[kDurPerLane], fd[kDurPerLane];
   LV al = {}, be = {}, ll = {};
-  double sc = 0.0;
+  float sc = 0.0f;
   int usable = 0;
   float lse_t = 0.0f, lse_d = 0.0f, fb = 0.0f, fl = 0.0f;
   long long y = -1;
@@ -134,8 +134,10 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
     return;
   }
   // c_b N with N = exp(alpha + beta - logL) = 2^((m_a + m_b - m_L) log2 e) s_a s_b / s_L
+  // (the fx difference converted with two 32-bit conversions: a 64-bit one
+  // runs at the float64 rate)
   const float a0 =
-      (float)sc * (fast_exp2(__ll2float_rn(al.m + be.m - ll.m) * kFxToLog2) * (al.s * be.s / ll.s));
+      sc * (fast_exp2(fx_diff_log2(al.m + be.m - ll.m)) * (al.s * be.s / ll.s));
   const float a = a0 * gs, lse2 = lse_t * kLog2e, lsed2 = lse_d * kLog2e;
   const float ab = (a0 * fb) * gs, alb = (a0 * fl) * gs;
   auto g_at = [&](float x, long long k) {

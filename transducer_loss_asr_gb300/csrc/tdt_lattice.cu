@@ -87,7 +87,7 @@ __device__ void write_utterance_info(const Problem &p, const Workspace &ws, long
   if (p.reduction == kMean) c = 1.0 / ((double)p.B * (double)p.label_lens[b]);
   else if (p.reduction == kMeanBatch) c = 1.0 / (double)p.B;
   else if (p.reduction == kMeanVolume) c = 1.0 / sum_u;
-  ws.scale[b] = c;
+  ws.scale[b] = (float)c;
   if (!ok) {
     LV z;
     z.m = 0;
