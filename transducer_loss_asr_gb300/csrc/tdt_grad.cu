@@ -14,12 +14,12 @@
 // more): each thread issues kBatch independent 16-byte loads, then computes
 // and stores them as 16-byte vectors, when the input row and the output row
 // sit at the same offset from a 16-byte boundary (the contiguous case);
-// otherwise (a strided view) output-aligned 16-byte vectors assembled from
-// the two aligned input vectors each one spans.  The row's coefficients (N, fB, fL,
-// fD_i, the saved log-sum-exps, the label) are read from the lattice pass's
-// outputs together with the row's first batch of logits, so their latencies
-// overlap; every lane of a row group computes them (the loads are
-// broadcasts within a warp).
+// otherwise (a strided view) it stores output-aligned 16-byte vectors, each
+// assembled from the two aligned input vectors it spans.  The row's
+// coefficients (N, fB, fL, fD_i, the saved log-sum-exps, the label) are read
+// from the lattice pass's outputs together with the row's first batch of
+// logits, so their latencies overlap; every lane of a row group computes
+// them (the loads are broadcasts within a warp).
 #include "tdt_rowio.cuh"
 
 namespace tdt {
