@@ -16,11 +16,13 @@
 //    direction forming a thread-block cluster.  G lanes serve one node (lane
 //    k takes durations k, k+G, ...).  A CTA keeps the values of the last RA
 //    diagonals of its rows in a shared ring, and the arc records of the
-//    diagonals in flight in a second ring that cp.async fills kPrefetch
-//    diagonals ahead, so no global round trip sits on the diagonal-to-
-//    diagonal path.  K is the fewest bands whose rings fit one CTA: a
-//    diagonal step is latency-bound, so splitting rows does not shorten it.
-//    With K = 1 (U+1 up to ~128) the kernel is compiled without any exchange.
+//    diagonals in flight in a second ring filled with cp.async P diagonals
+//    ahead (with several bands by the control warp, a diagonal's records of
+//    the band's rows being one contiguous block in the anti-diagonal layout;
+//    with one band by each node's lanes), so no global round trip sits on
+//    the diagonal-to-diagonal path.  K: one band up to 16 compute warps,
+//    else bands of ~12 warps (then the fewest whose rings fit).  With K = 1
+//    the kernel is compiled without any exchange.
 //    With K > 1 the one row a band needs from its neighbour (u_lo - 1 for
 //    alpha, u_hi + 1 for beta) is pushed into the neighbour's ring through
 //    distributed shared memory after every diagonal (st.async counted on an
@@ -389,9 +391,32 @@ size_t cluster_smem_bytes(int RA, int RW, int Rc, int rec) {
   return (size_t)RA * (Rc + 2) * sizeof(LV) + (size_t)RW * (Rc + 1) * rec * 8 + 2 * (size_t)RA * 8;
 }
 
-// Copy diagonal q's record of lattice row u (if it is a lattice node) into
-// the record ring: lane k copies the 16-byte chunks k, k+G, ...; every lane
-// commits one group per call so the group count per step is uniform.
+// Copy the arc records of diagonal q for ring rows 0 .. Rc (lattice rows
+// u_lo - 1 .. u_lo + Rc - 1, clipped to 0 .. U1 - 1) into the record ring.
+// In the anti-diagonal layout they are one contiguous block in global memory,
+// copied by the 32 lanes of one warp in 16-byte chunks (rows outside the
+// lattice come along and are never used).  Every lane of that warp commits
+// one group per call, so its group count per step is uniform; the other
+// warps issue no copies.
+template <int REC>
+__device__ __forceinline__ void prefetch_diag(const fx_t *gdiag0, const ClusterRings<REC> &r,
+                                              int q, int u_lo, int Rc, int U1, int nsteps,
+                                              int lane) {
+  if (q >= 0 && q < nsteps) {
+    const int u0 = u_lo - 1 > 0 ? u_lo - 1 : 0;
+    const int u1 = u_lo + Rc - 1 < U1 - 1 ? u_lo + Rc - 1 : U1 - 1;
+    const int nch = (u1 - u0 + 1) * (REC / 2);
+    const fx_t *src = gdiag0 + ((long long)q * U1 + u0) * REC;
+    fx_t *dst = r.w_mut(q, u0 - (u_lo - 1));
+    for (int c = lane; c < nch; c += 32) cp_async16(dst + 2 * c, src + 2 * c);
+  }
+  cp_async_commit();
+}
+
+// One band: each node's lanes copy the node's own record of diagonal q (if
+// it is a lattice node): lane k copies the 16-byte chunks k, k+G, ...; every
+// lane commits one group per call so the group count per step is uniform.
+// (Measured faster than one copying warp when there is no control warp.)
 template <int REC, int G>
 __device__ __forceinline__ void prefetch_rec(const fx_t *gdiag0, const ClusterRings<REC> &r,
                                              int q, int u, int ring_row, int k, int Tb, int Ub,
@@ -451,7 +476,10 @@ struct Band {
   int Rc, u_lo;   // rows [u_lo, u_lo + Rc)
   int row, lane;  // this thread's ring row (0 .. Rc; larger = idle) and lane
   bool control;       // the thread of the control warp that waits and releases
-  bool control_warp;  // a thread of that warp (no compute, no copies)
+  bool control_warp;  // a thread of that warp (no compute)
+  bool prefetch_warp; // a thread of the warp that copies the arc records
+                      // (the control warp; with one band each node's lanes
+                      // copy its own record)
   int Tb, Ub, U1;
   int *abort;     // shared flag, set after the loop: a bounded wait gave up
 };
@@ -464,8 +492,8 @@ struct Band {
 //                arrives after the barrier that ends its last read of j
 // Step j's halo value is read at steps j+1 .. j+1+max_dur, so it is released
 // at step j+2+max_dur; the producer of step j waits for the release of step
-// j - RA before storing.  The control warp issues no copies, no global
-// stores and no compute.
+// j - RA before storing.  The control warp issues no global stores and no
+// compute; it copies the arc records into the record ring.
 
 template <int ND, int G, bool MULTI, int P>
 __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace &ws,
@@ -488,13 +516,20 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     dd[j] = di[j] < ND ? p.dur[di[j]] : -1;
   }
   const int nsteps = bd.Tb + bd.Ub;
-  const bool pref = row <= cp.Rc && !(MULTI && bd.control_warp);
+  const bool pref = MULTI ? bd.prefetch_warp : row <= cp.Rc;
+  const int plane = threadIdx.x & 31;
   const bool producer = upper && row == cp.Rc && k == 0;  // feeds the upper band
   int failed = 0;  // a bounded wait of this thread gave up
-  for (int q = 0; q < P; ++q)
-    prefetch_rec<REC, G>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
+  auto prefetch = [&](int q) {
+    if (MULTI) {
+      if (pref) prefetch_diag<REC>(gdiag0, r, q, bd.u_lo, cp.Rc, bd.U1, nsteps, plane);
+    } else {
+      prefetch_rec<REC, G>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
+    }
+  };
+  for (int q = 0; q < P; ++q) prefetch(q);
   for (int s = 0; s < nsteps; ++s) {
-    prefetch_rec<REC, G>(gdiag0, r, s + P, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
+    prefetch(s + P);
     cp_async_wait<P>();
     if (MULTI && bd.control && lower && s >= 1) {
       // the lower band's value of diagonal s - 1
@@ -574,14 +609,21 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
   }
   const int nsteps = bd.Tb + bd.Ub;
   const int last = nsteps - 1;
-  const bool pref = own && !(MULTI && bd.control_warp);
+  const bool pref = MULTI ? bd.prefetch_warp : own;
+  const int plane = threadIdx.x & 31;
   const bool producer = lower && row == 1 && k == 0;  // feeds the lower band
   int failed = 0;  // a bounded wait of this thread gave up
-  for (int i = 0; i < P; ++i)
-    prefetch_rec<REC, G>(gdiag0, r, last - i, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
+  auto prefetch = [&](int q) {
+    if (MULTI) {
+      if (pref) prefetch_diag<REC>(gdiag0, r, q, bd.u_lo, cp.Rc, bd.U1, nsteps, plane);
+    } else {
+      prefetch_rec<REC, G>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
+    }
+  };
+  for (int i = 0; i < P; ++i) prefetch(last - i);
   for (int i = 0; i < nsteps; ++i) {
     const int q = last - i;
-    prefetch_rec<REC, G>(gdiag0, r, q - P, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
+    prefetch(q - P);
     cp_async_wait<P>();
     if (MULTI && bd.control && upper && i >= 1) {
       // the upper band's value of step i - 1 (diagonal q + 1)
@@ -658,8 +700,9 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
   }
 }
 
-// Block: (Rc + 1) * G compute threads (rounded up to whole warps), then one
-// control warp when there are neighbouring bands.
+// Block: (Rc + 1) * G compute threads (rounded up to whole warps), then,
+// with neighbouring bands, one control warp: it copies the arc records and
+// waits for and releases the halo slots.
 template <int ND, int G, bool MULTI, int P>
 __global__ void __launch_bounds__(kLatticeMaxThreads, 1)
 lattice_cluster_kernel(Problem p, Workspace ws, long long b0, ClusterPlan cp) {
@@ -705,6 +748,7 @@ lattice_cluster_kernel(Problem p, Workspace ws, long long b0, ClusterPlan cp) {
   bd.lane = in_compute ? (int)threadIdx.x % G : 0;
   bd.control = (int)threadIdx.x == compute_threads;
   bd.control_warp = !in_compute;
+  bd.prefetch_warp = MULTI && !in_compute;
   bd.Tb = (int)p.logit_lens[b];
   bd.Ub = (int)p.label_lens[b];
   bd.U1 = (int)p.U1;
