@@ -392,20 +392,23 @@ size_t cluster_smem_bytes(int RA, int RW, int Rc, int rec) {
 }
 
 // Copy the arc records of diagonal q for ring rows 0 .. Rc (lattice rows
-// u_lo - 1 .. u_lo + Rc - 1, clipped to 0 .. U1 - 1) into the record ring.
-// In the anti-diagonal layout they are one contiguous block in global memory,
-// copied by the 32 lanes of one warp in 16-byte chunks (rows outside the
-// lattice come along and are never used).  Every lane of that warp commits
-// one group per call, so its group count per step is uniform; the other
-// warps issue no copies.
+// u_lo - 1 .. u_lo + Rc - 1) into the record ring, for the rows that are
+// lattice nodes on that diagonal (0 <= q - u < T_b, u <= U_b).  In the
+// anti-diagonal layout those records are one contiguous block in global
+// memory, copied by the 32 lanes of one warp in 16-byte chunks.  Every lane
+// of that warp commits one group per call, so its group count per step is
+// uniform; the other warps issue no copies.
 template <int REC>
 __device__ __forceinline__ void prefetch_diag(const fx_t *gdiag0, const ClusterRings<REC> &r,
-                                              int q, int u_lo, int Rc, int U1, int nsteps,
+                                              int q, int u_lo, int Rc, int U1, int Tb, int Ub,
                                               int lane) {
-  if (q >= 0 && q < nsteps) {
-    const int u0 = u_lo - 1 > 0 ? u_lo - 1 : 0;
-    const int u1 = u_lo + Rc - 1 < U1 - 1 ? u_lo + Rc - 1 : U1 - 1;
-    const int nch = (u1 - u0 + 1) * (REC / 2);
+  if (q >= 0 && q < Tb + Ub) {
+    int u0 = u_lo - 1 > 0 ? u_lo - 1 : 0;
+    int u1 = u_lo + Rc - 1 < U1 - 1 ? u_lo + Rc - 1 : U1 - 1;
+    if (u0 < q - Tb + 1) u0 = q - Tb + 1;
+    if (u1 > q) u1 = q;
+    if (u1 > Ub) u1 = Ub;
+    const int nch = u1 >= u0 ? (u1 - u0 + 1) * (REC / 2) : 0;
     const fx_t *src = gdiag0 + ((long long)q * U1 + u0) * REC;
     fx_t *dst = r.w_mut(q, u0 - (u_lo - 1));
     for (int c = lane; c < nch; c += 32) cp_async16(dst + 2 * c, src + 2 * c);
@@ -522,7 +525,7 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
   int failed = 0;  // a bounded wait of this thread gave up
   auto prefetch = [&](int q) {
     if (MULTI) {
-      if (pref) prefetch_diag<REC>(gdiag0, r, q, bd.u_lo, cp.Rc, bd.U1, nsteps, plane);
+      if (pref) prefetch_diag<REC>(gdiag0, r, q, bd.u_lo, cp.Rc, bd.U1, bd.Tb, bd.Ub, plane);
     } else {
       prefetch_rec<REC, G>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
     }
@@ -615,7 +618,7 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
   int failed = 0;  // a bounded wait of this thread gave up
   auto prefetch = [&](int q) {
     if (MULTI) {
-      if (pref) prefetch_diag<REC>(gdiag0, r, q, bd.u_lo, cp.Rc, bd.U1, nsteps, plane);
+      if (pref) prefetch_diag<REC>(gdiag0, r, q, bd.u_lo, cp.Rc, bd.U1, bd.Tb, bd.Ub, plane);
     } else {
       prefetch_rec<REC, G>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
     }
