@@ -287,7 +287,7 @@ def run_decode(args, w, inp, dev, world, rank, dist):
             "value": ms, "unit": "ms", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
-            "config": dict(config_dict(w, "flushed between timed steps (2x L2 write)"),
+            "config": dict(config_dict(w, "flushed between timed steps (2x L2 write)", world),
                            max_symbols=args.max_symbols),
             "tokens_per_batch": tokens, "tokens_per_s": world * tokens / (ms / 1e3),
             "roofline": {"bound": "latency", "note": "one dependent row read and block argmax "
@@ -298,13 +298,17 @@ def run_decode(args, w, inp, dev, world, rank, dist):
     return 0
 
 
-def config_dict(w, l2):
+def config_dict(w, l2, world=1):
+    """The workload per rank; with N ranks each runs its own replica (the loss
+    shards by utterance), so the global batch is N x B."""
     return {"workload": "%s: B%d T%d U%d V%d D%d %s [%d,%d,%d,%d]%s, sigma %g, %s" % (
         w.name, w.B, w.T, w.U, w.V, w.D, w.dtype, w.B, w.T, w.U + 1, w.VD,
         " view of width %d" % w.base_vd if w.base_vd else "", w.sigma, w.reduction),
         "lengths": "full" if w.T_range is None else "T_b in %s, U_b in %s" % (w.T_range,
                                                                              w.U_range),
-        "l2": l2, "global_batch": w.B, "loss": w.loss}
+        "l2": l2, "global_batch": w.B * world, "loss": w.loss,
+        "parallelism": "one GPU" if world == 1 else
+                       "dp%d: one replica per GPU, no data-path collective" % world}
 
 
 def main():
@@ -528,7 +532,7 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": w.dtype, "data": "synthetic",
-            "config": config_dict(w, "flushed between timed steps (2x L2 write)"),
+            "config": config_dict(w, "flushed between timed steps (2x L2 write)", world),
             "frac_of_hbm_roofline": step_frac,
             "nominal_hbm_gbs": nominal_hbm_gbs(dev),
             "algorithmic_bytes_per_step": step_bytes,
