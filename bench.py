@@ -509,6 +509,15 @@ def main():
         per_kernel["node_tables"]["achieved_gbs"] = read_b * args.steps / (span_t / 1e3) / 1e9
     if roofline:
         per_kernel["grad"]["achieved_gbs"] = roofline["achieved"]
+    # the lattice passes are latency-bound: T_b + U_b dependent anti-diagonal
+    # steps per utterance (alpha and beta run side by side); report the time
+    # per step of the longest utterance of a launch
+    if "lattice" in per_kernel and per_kernel["lattice"]["launches"]:
+        steps = int((inp["logit_lens"].clamp(max=w.T) + inp["label_lens"].clamp(max=w.U)).max())
+        per_kernel["lattice"]["bound"] = "latency"
+        per_kernel["lattice"]["diagonal_steps"] = steps
+        per_kernel["lattice"]["us_per_diagonal_step"] = (
+            per_kernel["lattice"]["ms_per_launch"] * 1e3 / max(steps, 1))
     step_frac = (step_bytes / (ms_per_step / 1e3) / 1e9) / peak
 
     cpu = None
