@@ -31,6 +31,18 @@ constexpr int kBatch = 8;          // 16-byte loads issued per thread before use
 constexpr int kVecPerThread = 16;  // row vectors per thread when choosing TPR
 
 
+// (b, t, u) of row slot k when each utterance's T * U1 rows are walked
+// u-major: k = (b * U1 + u) * T + t; 32-bit divisions as above.
+__device__ __forceinline__ void decode_slot_umajor(const Problem &p, long long k, long long *b,
+                                                   long long *t, long long *u) {
+  const unsigned kk = (unsigned)k, U1 = (unsigned)p.U1, T = (unsigned)p.T;
+  const unsigned bu = kk / T;
+  *t = kk - bu * T;
+  const unsigned bb = bu / U1;
+  *u = bu - bb * U1;
+  *b = bb;
+}
+
 __device__ __forceinline__ fx_t clamp_lp(fx_t v) {
   const fx_t floor_fx = (fx_t)kLogProbFloor * (fx_t)4294967296LL;
   return v < floor_fx ? floor_fx : v;
@@ -121,11 +133,18 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
   __shared__ float sm_m[kTablesThreads / 32], sm_s[kTablesThreads / 32];
   const E *logits = static_cast<const E *>(p.logits);
   const int lt = threadIdx.x % TPR;
-  const long long n = n_begin + (long long)blockIdx.x * RPB + threadIdx.x / TPR;
-  long long b = 0, t = 0, u = 0, Ub = 0;
-  bool active = n < n_end;
+  // The row slots of a launch walk each utterance u-major (t fastest), so
+  // the RPB rows of a block share u and, with ragged label lengths, a block
+  // is either all padding (u > U_b, it ends at once) or all lattice rows
+  // instead of a few active rows among padding ones (measured: bf16 sliced
+  // workload 0.360 vs 0.367 ms, large_batch 1.903 vs 1.914 ms, parakeet
+  // unchanged).  A launch covers whole utterances.
+  const long long slot = n_begin + (long long)blockIdx.x * RPB + threadIdx.x / TPR;
+  long long b = 0, t = 0, u = 0, Ub = 0, n = 0;
+  bool active = slot < n_end;
   if (active) {
-    decode_node(p, n, &b, &t, &u);
+    decode_slot_umajor(p, slot, &b, &t, &u);
+    n = (b * p.T + t) * p.U1 + u;
     const long long Tb = p.logit_lens[b];
     Ub = p.label_lens[b];
     active = Tb >= 1 && Tb <= p.T && Ub >= 0 && Ub <= p.U1 - 1 && t < Tb && u <= Ub;
