@@ -540,8 +540,13 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
       arrive_expect_tx(f, (unsigned)sizeof(LV));
       if (!wait_parity_bounded(f, ((s - 1) / r.RA) & 1)) failed = 1;
     }
-    if (!MULTI) __syncthreads();
-    else if (__syncthreads_or(failed)) break;
+    // a thread whose wait gave up raises the CTA's abort flag before the
+    // barrier (every write to it precedes one), and all leave together after
+    // it; a plain barrier and a flag read cost less per diagonal than a
+    // barrier with a reduction (measured: long_labels lattice 4.79 vs 4.85 ms)
+    if (MULTI && failed) *bd.abort = 1;
+    __syncthreads();
+    if (MULTI && *bd.abort) break;
     // every thread is past step s - 1: release diagonal s - 2 - max_dur
     if (MULTI && bd.control && lower && s - 2 - p.max_dur >= 0)
       arrive_cluster_relaxed(map_cta(r.empty((s - 2 - p.max_dur) & r.mA), bd.k - 1));
@@ -634,8 +639,13 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
       arrive_expect_tx(f, (unsigned)sizeof(LV));
       if (!wait_parity_bounded(f, ((i - 1) / r.RA) & 1)) failed = 1;
     }
-    if (!MULTI) __syncthreads();
-    else if (__syncthreads_or(failed)) break;
+    // a thread whose wait gave up raises the CTA's abort flag before the
+    // barrier (every write to it precedes one), and all leave together after
+    // it; a plain barrier and a flag read cost less per diagonal than a
+    // barrier with a reduction (measured: long_labels lattice 4.79 vs 4.85 ms)
+    if (MULTI && failed) *bd.abort = 1;
+    __syncthreads();
+    if (MULTI && *bd.abort) break;
     // every thread is past step i - 1: release step i - 2 - max_dur
     if (MULTI && bd.control && upper && i - 2 - p.max_dur >= 0)
       arrive_cluster_relaxed(map_cta(r.empty((i - 2 - p.max_dur) & r.mA), bd.k + 1));
