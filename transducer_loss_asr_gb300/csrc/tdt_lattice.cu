@@ -531,14 +531,18 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     }
   };
   for (int q = 0; q < P; ++q) prefetch(q);
+  // halo slots armed ahead (arrive + expect 16 bytes): the first use of
+  // every slot now, each later use right after the previous one was waited
+  // for, past the barrier, so only the wait sits before it
+  if (MULTI && bd.control && lower)
+    for (int j = 0; j < r.RA && j <= nsteps - 2; ++j)
+      arrive_expect_tx(r.full(j), (unsigned)sizeof(LV));
   for (int s = 0; s < nsteps; ++s) {
     prefetch(s + P);
     cp_async_wait<P>();
     if (MULTI && bd.control && lower && s >= 1) {
       // the lower band's value of diagonal s - 1
-      unsigned long long *f = r.full((s - 1) & r.mA);
-      arrive_expect_tx(f, (unsigned)sizeof(LV));
-      if (!wait_parity_bounded(f, ((s - 1) / r.RA) & 1)) failed = 1;
+      if (!wait_parity_bounded(r.full((s - 1) & r.mA), ((s - 1) / r.RA) & 1)) failed = 1;
     }
     // a thread whose wait gave up raises the CTA's abort flag before the
     // barrier (every write to it precedes one), and all leave together after
@@ -547,6 +551,9 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     if (MULTI && failed) *bd.abort = 1;
     __syncthreads();
     if (MULTI && *bd.abort) break;
+    // the slot of diagonal s - 1 serves diagonal s - 1 + RA next
+    if (MULTI && bd.control && lower && s >= 1 && s - 1 + r.RA <= nsteps - 2)
+      arrive_expect_tx(r.full((s - 1) & r.mA), (unsigned)sizeof(LV));
     // every thread is past step s - 1: release diagonal s - 2 - max_dur
     if (MULTI && bd.control && lower && s - 2 - p.max_dur >= 0)
       arrive_cluster_relaxed(map_cta(r.empty((s - 2 - p.max_dur) & r.mA), bd.k - 1));
@@ -629,15 +636,17 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     }
   };
   for (int i = 0; i < P; ++i) prefetch(last - i);
+  // halo slots armed ahead, as in the alpha pass
+  if (MULTI && bd.control && upper)
+    for (int j = 0; j < r.RA && j <= nsteps - 2; ++j)
+      arrive_expect_tx(r.full(j), (unsigned)sizeof(LV));
   for (int i = 0; i < nsteps; ++i) {
     const int q = last - i;
     prefetch(q - P);
     cp_async_wait<P>();
     if (MULTI && bd.control && upper && i >= 1) {
       // the upper band's value of step i - 1 (diagonal q + 1)
-      unsigned long long *f = r.full((i - 1) & r.mA);
-      arrive_expect_tx(f, (unsigned)sizeof(LV));
-      if (!wait_parity_bounded(f, ((i - 1) / r.RA) & 1)) failed = 1;
+      if (!wait_parity_bounded(r.full((i - 1) & r.mA), ((i - 1) / r.RA) & 1)) failed = 1;
     }
     // a thread whose wait gave up raises the CTA's abort flag before the
     // barrier (every write to it precedes one), and all leave together after
@@ -646,6 +655,9 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     if (MULTI && failed) *bd.abort = 1;
     __syncthreads();
     if (MULTI && *bd.abort) break;
+    // the slot of step i - 1 serves step i - 1 + RA next
+    if (MULTI && bd.control && upper && i >= 1 && i - 1 + r.RA <= nsteps - 2)
+      arrive_expect_tx(r.full((i - 1) & r.mA), (unsigned)sizeof(LV));
     // every thread is past step i - 1: release step i - 2 - max_dur
     if (MULTI && bd.control && upper && i - 2 - p.max_dur >= 0)
       arrive_cluster_relaxed(map_cta(r.empty((i - 2 - p.max_dur) & r.mA), bd.k + 1));
