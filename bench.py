@@ -436,40 +436,63 @@ def main():
     # end to end through host buffers: the step's inputs host -> device from
     # pinned memory, the call, the step's result (the loss) device -> host;
     # the gradient stays on the device, where the backward pass of the joint
-    # network consumes it
+    # network consumes it.  Two device input buffers: step i + 1's copy (on a
+    # copy stream) runs while step i computes, as a data loader would; every
+    # step's copy and loss read lie inside the timed region.
     e2e_steps = args.e2e_steps or min(args.steps, 20)
     base = logits._base if logits._base is not None else logits
     base_h = torch.empty(base.shape, dtype=base.dtype, pin_memory=True)
     base_h.copy_(base)
-    base_d = torch.empty_like(base)
-    view_d = base_d[..., : w.VD] if base is not logits else base_d
     labels_h = inp["labels"].cpu().pin_memory()
     tl_h = inp["logit_lens"].cpu().pin_memory()
     ul_h = inp["label_lens"].cpu().pin_memory()
-    labels_d, tl_d, ul_d = (torch.empty_like(inp["labels"]), torch.empty_like(inp["logit_lens"]),
-                            torch.empty_like(inp["label_lens"]))
+    bufs = []
+    for _ in range(2):
+        base_d = torch.empty_like(base)
+        bufs.append((base_d, base_d[..., : w.VD] if base is not logits else base_d,
+                     torch.empty_like(inp["labels"]), torch.empty_like(inp["logit_lens"]),
+                     torch.empty_like(inp["label_lens"])))
     loss_h = torch.empty(loss.shape, dtype=loss.dtype, pin_memory=True)
     h2d = (base_h.numel() * base_h.element_size() + labels_h.numel() * 8 + tl_h.numel() * 8
            + ul_h.numel() * 8)
     d2h = loss_h.numel() * 4
+    compute = torch.cuda.current_stream()
+    copier = torch.cuda.Stream()
+    ready = [torch.cuda.Event(), torch.cuda.Event()]   # buffer k holds its step's inputs
+    free = [torch.cuda.Event(), torch.cuda.Event()]    # the call that read buffer k is done
 
-    def e2e_step():
-        base_d.copy_(base_h, non_blocking=True)
-        labels_d.copy_(labels_h, non_blocking=True)
-        tl_d.copy_(tl_h, non_blocking=True)
-        ul_d.copy_(ul_h, non_blocking=True)
-        call(view_d, labels_d, tl_d, ul_d)
-        loss_h.copy_(loss, non_blocking=True)
+    def copy_in(k, first_use):
+        base_d, _, labels_d, tl_d, ul_d = bufs[k]
+        with torch.cuda.stream(copier):
+            if not first_use:
+                copier.wait_event(free[k])
+            base_d.copy_(base_h, non_blocking=True)
+            labels_d.copy_(labels_h, non_blocking=True)
+            tl_d.copy_(tl_h, non_blocking=True)
+            ul_d.copy_(ul_h, non_blocking=True)
+            ready[k].record(copier)
 
-    for _ in range(3):
-        e2e_step()
+    def e2e_run(n):
+        copier.wait_stream(compute)
+        copy_in(0, True)
+        for i in range(n):
+            k = i & 1
+            if i + 1 < n:
+                copy_in(k ^ 1, i == 0)
+            compute.wait_event(ready[k])
+            _, view_d, labels_d, tl_d, ul_d = bufs[k]
+            call(view_d, labels_d, tl_d, ul_d)
+            free[k].record(compute)
+            loss_h.copy_(loss, non_blocking=True)
+        compute.wait_stream(copier)
+
+    e2e_run(3)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if dist is not None:
         dist.barrier()
     e0.record()
-    for _ in range(e2e_steps):
-        e2e_step()
+    e2e_run(e2e_steps)
     e1.record()
     torch.cuda.synchronize()
     e2e_ms = torch.tensor([e0.elapsed_time(e1) / e2e_steps], dtype=torch.float64, device=dev)
