@@ -107,10 +107,11 @@ extern "C" {
  * Loss and gradient in one call.  Internal scratch (per-node tables, alpha,
  * beta; tdt_loss_workspace_size bytes) is taken from the stream-ordered
  * allocator (cudaMallocAsync / cudaFreeAsync on `stream`).
- * Work is spread over a few internal streams of the current device (created
- * once per device, of several priorities) that fork from `stream` and join
- * back to it through events, so the call stays ordered on `stream` and can
- * be captured into a CUDA graph.  Calls on one device are enqueued one at a
+ * When the logits reach 8 MiB, the work is spread over a few internal
+ * streams of the current device (created once per device, of several
+ * priorities) that fork from `stream` and join back to it through events,
+ * so the call stays ordered on `stream` and can be captured into a CUDA
+ * graph; smaller problems run their kernels one after another on `stream`.  Calls on one device are enqueued one at a
  * time (an internal lock); their GPU work is ordered by the internal streams
  * and events.
  * Returns TDT_OK or a TDT_ERR_* status.

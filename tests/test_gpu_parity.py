@@ -128,6 +128,32 @@ def test_medium_cases(binding, oracle_mod, name):
     full_check(binding, oracle_mod, make_inputs(w, device="cuda"))
 
 
+# Problems whose logits reach 8 MiB go through the chunked multi-stream
+# schedule (up to four chunks of utterances); smaller ones run serially on the
+# caller's stream.  These cases sit above that size: B=5 splits unevenly into
+# chunks of 1,1,1,2 utterances, B=2 into two chunks and B=1 into one.
+CHUNKED = {
+    "f32_b5_ragged_view": dict(B=5, T=24, U=6, V=8193, blank=8192, durations=(0, 1, 2, 3, 4),
+                               dtype="f32", std=1.0, sigma=0.05, reduction="mean_volume",
+                               T_range=(12, 24), U_range=(2, 6), base_vd=8203),
+    "bf16_b4_ragged_view": dict(B=4, T=30, U=8, V=8193, blank=8192, durations=(0, 1, 2, 3),
+                                dtype="bf16", std=1.5, sigma=0.0, reduction="mean_batch",
+                                T_range=(15, 30), U_range=(1, 8), base_vd=8205),
+    "f16_b2_full": dict(B=2, T=30, U=8, V=16001, blank=16000, durations=(0, 1, 2),
+                        dtype="f16", std=1.0, sigma=0.02, reduction="sum"),
+    "f32_b1_full": dict(B=1, T=50, U=10, V=4097, blank=4096, durations=(0, 1, 2, 3, 4),
+                        dtype="f32", std=1.0, sigma=0.0, reduction="none"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CHUNKED))
+def test_chunked_schedule_cases(binding, oracle_mod, name):
+    w = scaled(WORKLOADS["tiny"], name=name, seed=919, **CHUNKED[name])
+    esize = 4 if w.dtype == "f32" else 2
+    assert w.B * w.T * (w.U + 1) * w.VD * esize >= 8 << 20
+    full_check(binding, oracle_mod, make_inputs(w, device="cuda"))
+
+
 @pytest.mark.parametrize("red", ["none", "sum", "mean", "mean_batch", "mean_volume"])
 def test_every_reduction(binding, oracle_mod, red):
     w = scaled(WORKLOADS["tiny"], name="red_" + red, B=5, T=14, U=5, V=50, blank=49,
@@ -314,13 +340,15 @@ def test_lattice_bands_do_not_change_results(binding, oracle_mod, name):
 
 # ------------------------------------------------------------- CUDA graphs
 
+@pytest.mark.parametrize("V", [200, 8193], ids=["serial", "chunked"])
 @pytest.mark.parametrize("own_workspace", [True, False])
-def test_cuda_graph_capture_and_replay(binding, own_workspace):
-    """The call is stream-ordered (the internal lattice streams fork from and
-    join back to the caller's stream through events), so it can be captured
-    into a CUDA graph; replays give the eager results, also after the inputs
-    change in place."""
-    w = scaled(WORKLOADS["tiny"], name="graph", B=3, T=21, U=6, V=200, blank=199,
+def test_cuda_graph_capture_and_replay(binding, own_workspace, V):
+    """The call is stream-ordered (small problems run on the caller's stream;
+    larger ones fork internal streams from it and join them back through
+    events), so it can be captured into a CUDA graph; replays give the eager
+    results, also after the inputs change in place.  V=8193 puts the logits
+    above the 8 MiB size of the chunked schedule."""
+    w = scaled(WORKLOADS["tiny"], name="graph", B=3, T=21, U=6, V=V, blank=V - 1,
                durations=(0, 1, 2, 3, 4), sigma=0.05, reduction="mean_volume",
                T_range=(10, 21), U_range=(2, 6), seed=606)
     inp = make_inputs(w, device="cuda")

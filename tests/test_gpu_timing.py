@@ -1,11 +1,13 @@
 """Per-kernel timing of the fused call (benchmark support), on the GPU.
 
-The call runs one K1 node-table pass, one lattice pass and one K4 gradient
-pass per chunk (up to four chunks of utterances) and one reduction.  The
-timing read returns, per kernel, the summed launch durations, the number of
-launches and the summed per-call busy window (first launch start to last
-launch end).  Checked: launch counts, positive times, a busy window at
-least as long as an average launch, and the reset.
+Problems whose logits reach 8 MiB run the chunked schedule: one K1
+node-table pass, one lattice pass and one K4 gradient pass per chunk (up to
+four chunks of utterances) and one reduction.  Smaller ones run each kernel
+once, serially on the caller's stream.  The timing read returns, per kernel,
+the summed launch durations, the number of launches and the summed per-call
+busy window (first launch start to last launch end).  Checked: launch
+counts on both paths, positive times, a busy window at least as long as an
+average launch, and the reset.
 """
 import pytest
 import torch
@@ -24,8 +26,9 @@ def binding():
     return b
 
 
-def test_timing_counts_and_busy_windows(binding):
-    w = scaled(WORKLOADS["parakeet"], name="timing", B=4, T=40, U=8, V=513, blank=512)
+@pytest.mark.parametrize("V,per_launch", [(8193, 4), (513, 1)], ids=["chunked", "serial"])
+def test_timing_counts_and_busy_windows(binding, V, per_launch):
+    w = scaled(WORKLOADS["parakeet"], name="timing", B=4, T=40, U=8, V=V, blank=V - 1)
     inp = make_inputs(w, device="cuda")
     calls = 3
     binding.tdt_loss_timing_read(reset=True)
@@ -39,7 +42,8 @@ def test_timing_counts_and_busy_windows(binding):
         kt = binding.tdt_loss_timing_read(reset=True)
     finally:
         binding.tdt_loss_timing_enable(False)
-    per_call = {"node_tables": 4, "lattice": 4, "reduce": 1, "grad": 4}
+    per_call = {"node_tables": per_launch, "lattice": per_launch, "reduce": 1,
+                "grad": per_launch}
     for name, n in per_call.items():
         ms, launches, busy = kt[name]
         assert launches == n * calls, (name, launches)

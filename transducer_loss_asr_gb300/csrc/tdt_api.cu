@@ -228,6 +228,7 @@ cudaError_t timed(int id, cudaStream_t stream, F fn) {
 
 // ---- per-device internal stream and events -----------------------------------
 constexpr int kChunks = 4;
+constexpr long long kSerialBytes = 8ll << 20;  // below: one stream, no chunks
 
 struct DeviceRes {
   bool ready = false;
@@ -286,12 +287,29 @@ int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void 
   const bool with_grad = grad_out != nullptr;
   coeffs = coeffs || with_grad;
   const long long rows_per_utt = p.T * p.U1;
-  const int nchunk = (int)(p.B < kChunks ? (p.B > 0 ? p.B : 1) : kChunks);
-  auto b_lo = [&](int c) { return p.B * c / nchunk; };
 #define TDT_TRY(x) \
   do {             \
     if ((x) != cudaSuccess) return TDT_ERR_CUDA; \
   } while (0)
+  // Small problems (logits below kSerialBytes): launch latency, not
+  // bandwidth, sets the time, so the kernels run one after another on the
+  // caller's stream with no fork, join or chunking.
+  const long long logit_bytes = p.B * rows_per_utt * p.VD * (dtype == kF32 ? 4 : 2);
+  if (logit_bytes < kSerialBytes) {
+    const long long rows = p.B * rows_per_utt;
+    TDT_TRY(timed(TDT_KERNEL_TABLES, stream,
+                  [&] { return launch_node_tables(p, dtype, ws, 0, rows, stream); }));
+    TDT_TRY(timed(TDT_KERNEL_LATTICE, stream,
+                  [&] { return launch_lattice(p, ws, 0, p.B, coeffs, stream); }));
+    TDT_TRY(timed(TDT_KERNEL_REDUCE, stream, [&] { return launch_reduce(p, ws, loss_out, stream); }));
+    if (with_grad)
+      TDT_TRY(timed(TDT_KERNEL_GRAD, stream, [&] {
+        return launch_grad(p, dtype, ws, grad_out, gscale, 0, rows, stream);
+      }));
+    return TDT_OK;
+  }
+  const int nchunk = (int)(p.B < kChunks ? (p.B > 0 ? p.B : 1) : kChunks);
+  auto b_lo = [&](int c) { return p.B * c / nchunk; };
   TDT_TRY(cudaEventRecord(res->fork, stream));
   for (int c = 0; c < nchunk; ++c) TDT_TRY(cudaStreamWaitEvent(res->side[c], res->fork, 0));
   const int nts = nchunk < 2 ? nchunk : 2;
