@@ -56,7 +56,7 @@ bool make_layout(const int64_t sizes[4], int n_dur, Layout *L) {
   L->beta = take(ndiag * sizeof(LV));
   L->lse_tok = take(nodes * 4);
   L->lse_dur = take(nodes * 4);
-  L->frac = take(nodes * 4 * (size_t)(2 + n_dur));
+  L->frac = take(ndiag * 4 * (size_t)(2 + n_dur));
   L->loglik = take((size_t)B * sizeof(LV));
   L->scale = take((size_t)B * 4);
   L->usable = take((size_t)B * 4);

@@ -90,11 +90,12 @@ struct Workspace {
   fx_t *arcw;    // [g][rec_len] node arc records (arc_record_len)
   LV *alpha;     // [g]
   LV *beta;      // [g]
+  float *frac;   // [g][2 + n_dur]: share of beta(t,u) through its blank arcs,
+                 //   its label arcs, and through each duration (a record per
+                 //   node, so the nodes of a diagonal write adjacent records)
   // node-major per-row data, index n = (b * T + t) * U1 + u
   float *lse_tok;  // log-sum-exp of the token logits
   float *lse_dur;  // log-sum-exp of the duration logits
-  float *frac;     // [(2 + D)][nodes]: share of beta(t,u) through blank arcs,
-                   //   label arcs, and through each duration
   // per utterance
   LV *loglik;      // [B] log-likelihood from alpha (s = 0: no path)
   float *scale;    // [B] c_b, factor of dL_b/dz in the reduced loss

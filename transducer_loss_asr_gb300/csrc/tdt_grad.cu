@@ -90,7 +90,6 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
   const long long tail0 = head + (long long)nvec * N;
   const int ntail = (int)(p.V - tail0);
   const uint4 *vin = reinterpret_cast<const uint4 *>(row + head);
-  const long long nodes = p.B * p.T * p.U1;
   uint4 v[kBatch];
   float zh = 0.0f, zt = 0.0f, zd[kDurPerLane], fd[kDurPerLane];
   LV al = {}, be = {}, ll = {};
@@ -108,13 +107,14 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
       if (lt < head) zh = ld_elem<DT, COH>(row + lt);
       if (lt < ntail) zt = ld_elem<DT, COH>(row + tail0 + lt);
     }
+    const long long q = diag_index(p, b, t, u);
+    const float *fr = ws.frac + q * (2 + p.n_dur);  // the node's fraction record
 #pragma unroll
     for (int c = 0; c < kDurPerLane; ++c) {
       const int i = lt + c * TPR;
       zd[c] = i < p.D ? ld_elem<DT, COH>(row + p.V + i) : 0.0f;
-      fd[c] = i < p.D ? ws.frac[(long long)(2 + i) * nodes + n] : 0.0f;
+      fd[c] = i < p.D ? fr[2 + i] : 0.0f;
     }
-    const long long q = diag_index(p, b, t, u);
     al = ws.alpha[q];
     be = ws.beta[q];
     ll = ws.loglik[b];
@@ -122,8 +122,8 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
     usable = ws.usable[b];
     lse_t = ws.lse_tok[n];
     lse_d = ws.lse_dur[n];
-    fb = ws.frac[n];
-    fl = ws.frac[nodes + n];
+    fb = fr[0];
+    fl = fr[1];
     if (u < Ub) y = p.labels[b * (p.U1 - 1) + u];
   }
   // upstream gradient of utterance b's loss (1 when none is given; x * 1 is exact)

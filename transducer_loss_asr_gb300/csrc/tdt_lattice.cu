@@ -187,19 +187,19 @@ __device__ void termination(const Problem &p, const Workspace &ws, long long b, 
 }
 
 // Shares of beta(t,u) through blank arcs, label arcs and each duration (arc
-// posteriors divided by the node occupancy), from the per-arc terms.
-__device__ __forceinline__ void write_fractions(const Problem &p, const Workspace &ws,
-                                                long long n, const float *term, float inv,
-                                                int nd) {
-  const long long nodes = p.B * p.T * p.U1;
+// posteriors divided by the node occupancy), from the per-arc terms, into
+// the fraction record of anti-diagonal slot g.
+__device__ __forceinline__ void write_fractions(const Workspace &ws, long long g,
+                                                const float *term, float inv, int nd) {
+  float *fr = ws.frac + g * (2 + nd);
   float fb = 0.0f, fl = 0.0f;
   for (int i = 0; i < nd; ++i) {
     fb += term[i];
     fl += term[nd + i];
-    ws.frac[(long long)(2 + i) * nodes + n] = (term[i] + term[nd + i]) * inv;
+    fr[2 + i] = (term[i] + term[nd + i]) * inv;
   }
-  ws.frac[n] = fb * inv;
-  ws.frac[nodes + n] = fl * inv;
+  fr[0] = fb * inv;
+  fr[1] = fl * inv;
 }
 
 // ---------------------------------------------------------------- fallback
@@ -292,7 +292,7 @@ beta_kernel(Problem p, Workspace ws, long long b0) {
       fx_t m;
       float sv, inv;
       lse_combine_n(M, S, 2 * nd, &m, &sv, term, &inv);
-      write_fractions(p, ws, (b * p.T + t) * p.U1 + u, term, inv, nd);
+      write_fractions(ws, q, term, inv, nd);
       ws.beta[q] = make_lv(m, sv);
     }
     __syncthreads();
@@ -615,7 +615,7 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
   const bool lower = MULTI && bd.k > 0, upper = MULTI && bd.k + 1 < bd.K;
   const fx_t *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * REC;
   LV *gbeta = ws.beta + b * p.n_diag * p.U1;
-  const long long nodes = p.B * p.T * p.U1;
+  float *gfrac = ws.frac + b * p.n_diag * p.U1 * (2 + ND);
   int di[J], dd[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) {
@@ -688,13 +688,13 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     group_lse<J, G>(M, S, &ms, &tot, term);
     const float inv = tot > 0.0f ? fast_rcp(tot) : 0.0f;
     float fb = 0.0f, fl = 0.0f;
-    const long long n = (b * p.T + t) * p.U1 + u;
+    // the node's fraction record; the nodes of a diagonal have adjacent ones
+    float *fr = gfrac + ((long long)q * bd.U1 + u) * (2 + ND);
 #pragma unroll
     for (int j = 0; j < J; ++j) {
       fb += term[2 * j];
       fl += term[2 * j + 1];
-      if (node && di[j] < ND)
-        ws.frac[(long long)(2 + di[j]) * nodes + n] = (term[2 * j] + term[2 * j + 1]) * inv;
+      if (node && di[j] < ND) fr[2 + di[j]] = (term[2 * j] + term[2 * j + 1]) * inv;
     }
 #pragma unroll
     for (int o = 1; o < G; o <<= 1) {
@@ -704,8 +704,8 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     const LV v = node ? lv_from_sum(tot, ms) : make_lv(kFxVeryNeg, 0.0f);
     if (own && k == 0) r.a(q, row) = v;
     if (node && k == 0) {
-      ws.frac[n] = fb * inv;
-      ws.frac[nodes + n] = fl * inv;
+      fr[0] = fb * inv;
+      fr[1] = fl * inv;
       gbeta[(long long)q * bd.U1 + u] = v;
     }
     if (producer) {
