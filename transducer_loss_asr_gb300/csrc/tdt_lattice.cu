@@ -99,38 +99,9 @@ __device__ void write_utterance_info(const Problem &p, const Workspace &ws, long
   }
 }
 
-// Log-sum-exp of N candidate arcs (M_j, S_j) (S_j = 0: no arc) into (m, s);
-// with TERMS also each arc's unnormalised term and 1 / their sum.
-template <int N, bool TERMS>
-__device__ __forceinline__ void lse_combine(const fx_t *M, const float *S, fx_t *m, float *s,
-                                            float *term, float *inv_total) {
-  fx_t ms = kFxNegInf;
-#pragma unroll
-  for (int j = 0; j < N; ++j)
-    if (S[j] > 0.0f) ms = fmax_fx(ms, M[j]);
-  if (ms == kFxNegInf) {
-    *m = 0;
-    *s = 0.0f;
-    if (TERMS) {
-#pragma unroll
-      for (int j = 0; j < N; ++j) term[j] = 0.0f;
-      *inv_total = 0.0f;
-    }
-    return;
-  }
-  float tot = 0.0f;
-#pragma unroll
-  for (int j = 0; j < N; ++j) {
-    float e = 0.0f;
-    if (S[j] > 0.0f) e = S[j] * fast_exp2(fx_diff_log2(M[j] - ms));
-    if (TERMS) term[j] = e;
-    tot += e;
-  }
-  lv_normalize(tot, ms, m, s);
-  if (TERMS) *inv_total = fast_rcp(tot);
-}
-
-// Same for a runtime number of candidates (n <= 2 * kMaxDurations).
+// Log-sum-exp of n candidate arcs (M_j, S_j) (S_j = 0: no arc) into (m, s);
+// with term non-null also each arc's unnormalised term and 1 / their sum
+// (n <= 2 * kMaxDurations).
 __device__ void lse_combine_n(const fx_t *M, const float *S, int n, fx_t *m, float *s,
                               float *term, float *inv_total) {
   fx_t ms = kFxNegInf;
