@@ -253,8 +253,16 @@ template <int DT>
 cudaError_t launch_dt(const Problem &p, const Workspace &ws, long long n_begin, long long n_end,
                       cudaStream_t stream) {
   // a warp per long row (no shared-memory combine), fewer lanes for short rows
-  int tpr = row_group_threads(p.V * (long long)sizeof(typename Elem<DT>::T), kVecPerThread);
+  const long long row_bytes = p.V * (long long)sizeof(typename Elem<DT>::T);
+  int tpr = row_group_threads(row_bytes, kVecPerThread);
   if (tpr > 32) tpr = 32;
+  // fp32 rows of up to 1 KB: 4 lanes (one 4-element vector of scalar head or
+  // tail per lane), so a warp's per-row work (the group combines, the
+  // duration softmax, the record) serves 8 rows instead of 4
+  if constexpr (Vec<DT>::N <= 4) {
+    if (row_bytes <= 4 * kVecPerThread * 16)
+      return launch_tpr<DT, 4>(p, ws, n_begin, n_end, stream);
+  }
   switch (tpr) {
     case 8: return launch_tpr<DT, 8>(p, ws, n_begin, n_end, stream);
     case 16: return launch_tpr<DT, 16>(p, ws, n_begin, n_end, stream);
