@@ -9,9 +9,10 @@
 // tail (tdt_rowio.cuh).  Each thread keeps a running max and a running sum
 // of exp(z - max) in fp32; the group combines them with shuffles ("Warp
 // Shuffle Reductions", "cuda-kernels" skill page) and, for groups wider than
-// a warp, through shared memory.  TPR grows with the row length (8 threads
-// for rows of ~140 floats, a warp from ~2000 floats up), so the per-row
-// work is amortised over many vectors per thread.
+// a warp, through shared memory.  TPR grows with the row length (4 threads
+// for fp32 rows of up to 256 floats, 8 for 16-bit rows of up to 1024, a
+// warp from ~2000 floats up), so the per-row work is amortised over many
+// vectors per thread.
 // The row may be a slice of a wider tensor: only strides s0..s2 locate it.
 //
 // Outputs per usable node (t < T_b, u <= U_b):
