@@ -46,3 +46,39 @@ def test_gpu_arm_fails_without_a_gpu():
              timeout=120)
     assert r.returncode != 0
     assert not [l for l in r.stdout.splitlines() if l.startswith("{")]
+
+
+def _bench_module():
+    import importlib.util
+
+    spec = importlib.util.spec_from_file_location("bench_under_test", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def test_algorithmic_bytes_counts_lattice_rows_read_and_every_row_written():
+    """The roofline's numerator: every logit of a lattice row (t < T_b,
+    u <= U_b) read once, every gradient element written once.  Checked
+    against an explicit enumeration of the rows on a ragged bf16 view, and
+    the parakeet figure from its sizes alone."""
+    from transducer_loss_asr_gb300.workloads import WORKLOADS, scaled
+
+    bench = _bench_module()
+    w = scaled(WORKLOADS["parakeet_bf16_ragged"], name="bytes", B=3, T=7, U=4, V=20, blank=19,
+               base_vd=30)
+    tl = torch.tensor([7, 3, 5])
+    ul = torch.tensor([4, 0, 2])
+    read_b, write_b, valid, rows = bench.algorithmic_bytes(
+        {"workload": w, "logit_lens": tl, "label_lens": ul})
+    lattice_rows = sum(1 for b in range(3) for t in range(7) for u in range(5)
+                       if t < int(tl[b]) and u <= int(ul[b]))
+    assert valid == lattice_rows == 7 * 5 + 3 * 1 + 5 * 3
+    assert rows == 3 * 7 * 5
+    assert read_b == lattice_rows * w.VD * 2 and write_b == rows * w.VD * 2
+    # parakeet fp32 [4, 200, 41, 8198], full lengths: 2 x 1,075,577,600 bytes
+    p = WORKLOADS["parakeet"]
+    read_b, write_b, _, _ = bench.algorithmic_bytes(
+        {"workload": p, "logit_lens": torch.full((4,), 200), "label_lens": torch.full((4,), 40)})
+    assert read_b == write_b == 1_075_577_600
+    assert read_b + write_b == 2_151_155_200
