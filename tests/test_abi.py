@@ -242,3 +242,21 @@ def test_greedy_decode_validates(lib):
     assert call(strides=(150, 30, 10, 3)) == -3
     assert call(logits=FAKE + 2) == -11
     assert call(sizes=(0, 5, 3, 10)) == 0  # empty batch: nothing to do, nothing touched
+
+
+def test_binding_import_fails_loudly_without_the_library(tmp_path):
+    """No fallback: a copy of the package without libtdt_loss.so cannot load
+    its binding; the error names the missing library and the build.  (The
+    autograd op imports the binding in its device implementation, so its
+    first CUDA call raises the same error.)"""
+    import shutil
+    import subprocess
+    import sys
+
+    src = os.path.join(ROOT, "transducer_loss_asr_gb300")
+    shutil.copytree(src, tmp_path / "transducer_loss_asr_gb300",
+                    ignore=shutil.ignore_patterns("*.so", "__pycache__", "csrc"))
+    r = subprocess.run([sys.executable, "-c", "import transducer_loss_asr_gb300.binding"],
+                       cwd=tmp_path, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "libtdt_loss.so is not built" in r.stderr
