@@ -227,8 +227,11 @@ int tdt_loss_bwd(const void *logits, const int64_t sizes[4], const int64_t strid
  *   - All calls on a device share the array: calls whose GPU work overlaps
  *     (other streams, unordered host threads) race.  Order them on one
  *     stream.  No entry of the array has to start at zero.
- *   - The first call on a device looks up the array's device address with
- *     that device current; make that first call before any stream capture.
+ *   - The first call in each CUDA context looks up the array's device
+ *     address with that context current and keeps it under the context's
+ *     unique id: the first call on a device, and again the first call after
+ *     cudaDeviceReset or with another context current.  Make that first
+ *     call before any stream capture.
  *   - The kernels run one after another on `stream`; no internal stream or
  *     event is created.
  */
@@ -279,6 +282,23 @@ int tdt_loss_timing_read(double *ms_out, int64_t *count_out, double *span_ms_out
  * previous setting.
  */
 int tdt_loss_set_lattice_bands(int bands);
+
+/*
+ * Testing support for the bounded waits of the multi-band lattice passes
+ * (failure detection; the pages have no counterpart).  When an utterance's
+ * rows are split into K >= 2 bands, each band waits for its neighbour's
+ * boundary row on every anti-diagonal, and every such wait gives up after a
+ * limit: the utterance then gets a NaN loss and zero gradient rows, and the
+ * call still returns normally.  With utterance >= 0, later calls run the
+ * lattice passes of that utterance index with band 1 never publishing its
+ * boundary row, so its neighbours' waits run out; every other utterance is
+ * computed as usual.  wait_limit_cycles > 0 sets the limit of every wait of
+ * later calls in GPU clock cycles (0: the default, about one second).
+ * utterance < 0 switches the fault off.  Process-wide; returns the previous
+ * utterance setting (-1: none).  Only multi-band lattices wait at all
+ * (tdt_loss_set_lattice_bands(K >= 2), or lattices too tall for one CTA).
+ */
+long long tdt_loss_test_set_halo_fault(long long utterance, long long wait_limit_cycles);
 
 /* Human-readable text for a status code (static storage). */
 const char *tdt_status_string(int status);

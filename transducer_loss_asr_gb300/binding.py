@@ -60,6 +60,8 @@ def _load() -> ctypes.CDLL:
     lib.tdt_loss_version.argtypes = []
     lib.tdt_loss_set_lattice_bands.restype = I
     lib.tdt_loss_set_lattice_bands.argtypes = [I]
+    lib.tdt_loss_test_set_halo_fault.restype = ctypes.c_longlong
+    lib.tdt_loss_test_set_halo_fault.argtypes = [ctypes.c_longlong, ctypes.c_longlong]
     lib.tdt_loss_timing_enable.restype = None
     lib.tdt_loss_timing_enable.argtypes = [I]
     lib.tdt_loss_timing_read.restype = I
@@ -276,6 +278,15 @@ def tdt_loss_set_lattice_bands(bands: int) -> int:
     """Force K bands (CTAs per utterance and direction) in the lattice passes;
     0 = automatic.  Results do not depend on K.  Returns the previous value."""
     return int(lib.tdt_loss_set_lattice_bands(int(bands)))
+
+
+def tdt_loss_test_set_halo_fault(utterance: int, wait_limit_cycles: int = 0) -> int:
+    """Testing: make the multi-band lattice passes of utterance index
+    ``utterance`` lose their band-1 boundary row so the neighbours' bounded
+    waits run out (NaN loss, zero gradient rows for that utterance only);
+    ``wait_limit_cycles`` > 0 shortens every wait's limit.  utterance < 0
+    switches it off.  Returns the previous utterance setting."""
+    return int(lib.tdt_loss_test_set_halo_fault(int(utterance), int(wait_limit_cycles)))
 
 
 KERNEL_NAMES = ("node_tables", "lattice", "reduce", "grad")

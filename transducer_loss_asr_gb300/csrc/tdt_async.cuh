@@ -49,12 +49,14 @@ __device__ __forceinline__ bool test_wait_parity(unsigned long long *bar, unsign
 }
 // About one second at the GB300 clock: far beyond any legitimate wait.
 constexpr long long kWaitLimitCycles = 2000000000LL;
-// Wait for the completion of the phase of parity `parity`; false on timeout.
-__device__ __forceinline__ bool wait_parity_bounded(unsigned long long *bar, unsigned parity) {
+// Wait for the completion of the phase of parity `parity` for at most
+// `limit` clock cycles; false on timeout.
+__device__ __forceinline__ bool wait_parity_bounded(unsigned long long *bar, unsigned parity,
+                                                    long long limit) {
   if (test_wait_parity(bar, parity)) return true;
   const long long t0 = clock64();
   while (!test_wait_parity(bar, parity))
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   return true;
 }
 

@@ -61,6 +61,10 @@ struct Problem {
   int rnnt;                       // 1: plain RNN-T: no duration logits (D = 0); the
                                   //    lattice durations are {0, 1} with blank arcs
                                   //    of duration 1 and label arcs of duration 0 only
+  long long wait_limit;           // clock cycles a lattice band waits for a neighbour
+                                  //    before it gives up (set by launch_lattice)
+  long long fault_utt;            // testing: the utterance whose band 1 never publishes
+                                  //    its boundary row (-1: none; set by launch_lattice)
 };
 
 // Node arc record (fx values), one per lattice node in anti-diagonal order:
@@ -99,7 +103,9 @@ struct Workspace {
   // per utterance
   LV *loglik;      // [B] log-likelihood from alpha (s = 0: no path)
   float *scale;    // [B] c_b, factor of dL_b/dz in the reduced loss
-  int *usable;     // [B] 1 = lengths and labels usable
+  int *usable;     // [B] 1 = usable: set to 1 by the node-table pass of the
+                   //   utterance's chunk, cleared by the lattice passes when the
+                   //   lengths or labels are unusable or a bounded wait gave up
 };
 
 __host__ __device__ inline long long diag_index(const Problem &p, long long b, long long t,

@@ -46,6 +46,11 @@ extern __shared__ __align__(16) unsigned char tdt_dyn_smem[];
 
 // Band count forced by tdt_loss_set_lattice_bands (0: chosen per problem).
 std::atomic<int> g_forced_bands{0};
+// Testing support (tdt_loss_test_set_halo_fault): the utterance whose band 1
+// withholds its boundary row (-1: none) and the wait limit in clock cycles
+// (0: kWaitLimitCycles).
+std::atomic<long long> g_fault_utt{-1};
+std::atomic<long long> g_wait_limit{0};
 
 namespace {
 
@@ -81,10 +86,13 @@ __device__ bool check_utterance(const Problem &p, long long b, double *sum_u_out
   return ok;
 }
 
-// Per-utterance outputs of the alpha side: usable flag and c_b.
+// Per-utterance outputs of the alpha side: c_b, and the usable flag cleared
+// for unusable lengths or labels (the node-table pass set it to 1 before this
+// launch; a pass whose bounded wait gives up also clears it, so the flag is
+// only ever cleared here, whatever order the clusters run in).
 __device__ void write_utterance_info(const Problem &p, const Workspace &ws, long long b, bool ok,
                                      double sum_u) {
-  ws.usable[b] = ok ? 1 : 0;
+  if (!ok) ws.usable[b] = 0;
   double c = 1.0;
   if (p.reduction == kMean) c = 1.0 / ((double)p.B * (double)p.label_lens[b]);
   else if (p.reduction == kMeanBatch) c = 1.0 / (double)p.B;
@@ -492,7 +500,9 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
   const int nsteps = bd.Tb + bd.Ub;
   const bool pref = MULTI ? bd.prefetch_warp : row <= cp.Rc;
   const int plane = threadIdx.x & 31;
-  const bool producer = upper && row == cp.Rc && k == 0;  // feeds the upper band
+  // feeds the upper band (testing: band 1 of utterance fault_utt never does,
+  // so the upper band's bounded wait runs out)
+  const bool producer = upper && row == cp.Rc && k == 0 && !(bd.k == 1 && b == p.fault_utt);
   int failed = 0;  // a bounded wait of this thread gave up
   auto prefetch = [&](int q) {
     if (MULTI) {
@@ -513,7 +523,8 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     cp_async_wait<P>();
     if (MULTI && bd.control && lower && s >= 1) {
       // the lower band's value of diagonal s - 1
-      if (!wait_parity_bounded(r.full((s - 1) & r.mA), ((s - 1) / r.RA) & 1)) failed = 1;
+      if (!wait_parity_bounded(r.full((s - 1) & r.mA), ((s - 1) / r.RA) & 1, p.wait_limit))
+        failed = 1;
     }
     // a thread whose wait gave up raises the CTA's abort flag before the
     // barrier (every write to it precedes one), and all leave together after
@@ -559,7 +570,8 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     if (producer) {
       // publish this diagonal's top row into the upper band's halo slot once
       // that band has released the slot's previous diagonal
-      if (s >= r.RA && !wait_parity_bounded(r.empty(s & r.mA), ((s / r.RA) - 1) & 1))
+      if (s >= r.RA &&
+          !wait_parity_bounded(r.empty(s & r.mA), ((s / r.RA) - 1) & 1, p.wait_limit))
         failed = 1;
       else
         st_async_lv(map_cta(&r.a(s, 0), bd.k + 1), v, map_cta(r.full(s & r.mA), bd.k + 1));
@@ -597,7 +609,8 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
   const int last = nsteps - 1;
   const bool pref = MULTI ? bd.prefetch_warp : own;
   const int plane = threadIdx.x & 31;
-  const bool producer = lower && row == 1 && k == 0;  // feeds the lower band
+  // feeds the lower band (testing: band 1 of utterance fault_utt never does)
+  const bool producer = lower && row == 1 && k == 0 && !(bd.k == 1 && b == p.fault_utt);
   int failed = 0;  // a bounded wait of this thread gave up
   auto prefetch = [&](int q) {
     if (MULTI) {
@@ -617,7 +630,8 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     cp_async_wait<P>();
     if (MULTI && bd.control && upper && i >= 1) {
       // the upper band's value of step i - 1 (diagonal q + 1)
-      if (!wait_parity_bounded(r.full((i - 1) & r.mA), ((i - 1) / r.RA) & 1)) failed = 1;
+      if (!wait_parity_bounded(r.full((i - 1) & r.mA), ((i - 1) / r.RA) & 1, p.wait_limit))
+        failed = 1;
     }
     // a thread whose wait gave up raises the CTA's abort flag before the
     // barrier (every write to it precedes one), and all leave together after
@@ -681,7 +695,8 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     }
     if (producer) {
       // publish this diagonal's bottom row into the lower band's halo slot
-      if (i >= r.RA && !wait_parity_bounded(r.empty(i & r.mA), ((i / r.RA) - 1) & 1))
+      if (i >= r.RA &&
+          !wait_parity_bounded(r.empty(i & r.mA), ((i / r.RA) - 1) & 1, p.wait_limit))
         failed = 1;
       else
         st_async_lv(map_cta(&r.a(q, cp.Rc + 1), bd.k - 1), v,
@@ -980,9 +995,13 @@ __global__ void reduce_kernel(Problem p, Workspace ws, float *loss_out) {
 }  // namespace
 
 
-cudaError_t launch_lattice(const Problem &p, const Workspace &ws, long long b_begin,
+cudaError_t launch_lattice(const Problem &p_in, const Workspace &ws, long long b_begin,
                            long long b_end, bool with_beta, cudaStream_t stream,
                            cudaEvent_t started, bool *started_used) {
+  Problem p = p_in;
+  const long long limit = g_wait_limit.load();
+  p.wait_limit = limit > 0 ? limit : kWaitLimitCycles;
+  p.fault_utt = g_fault_utt.load();
   if (started_used) *started_used = false;
   if (b_end - b_begin > 65535) started = nullptr;
   // grid.y is at most 65535: launch in groups of utterances
@@ -1025,4 +1044,10 @@ cudaError_t launch_reduce(const Problem &p, const Workspace &ws, float *loss_out
 extern "C" int tdt_loss_set_lattice_bands(int bands) {
   if (bands < 0) bands = 0;
   return tdt::g_forced_bands.exchange(bands);
+}
+
+extern "C" long long tdt_loss_test_set_halo_fault(long long utterance,
+                                                  long long wait_limit_cycles) {
+  tdt::g_wait_limit.store(wait_limit_cycles > 0 ? wait_limit_cycles : 0);
+  return tdt::g_fault_utt.exchange(utterance >= 0 ? utterance : -1);
 }

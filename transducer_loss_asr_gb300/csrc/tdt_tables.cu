@@ -21,6 +21,7 @@
 //                            and label arc log-weights per duration,
 //                            anti-diagonal layout, one contiguous record per
 //                            node for the lattice passes
+// and usable[b] = 1 for every utterance of the launch.
 #include "tdt_rowio.cuh"
 
 namespace tdt {
@@ -134,6 +135,14 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
   __shared__ float sm_m[kTablesThreads / 32], sm_s[kTablesThreads / 32];
   const E *logits = static_cast<const E *>(p.logits);
   const int lt = threadIdx.x % TPR;
+  // A launch covers whole utterances: mark them usable before their lattice
+  // passes run (those clear the flag of an utterance with unusable lengths or
+  // labels, or whose bounded wait gave up).
+  if (blockIdx.x == 0) {
+    const long long per_utt = p.T * p.U1;
+    for (long long bb = n_begin / per_utt + threadIdx.x; bb < n_end / per_utt; bb += blockDim.x)
+      ws.usable[bb] = 1;
+  }
   // The row slots of a launch walk each utterance u-major (t fastest), so
   // the RPB rows of a block share u and, with ragged label lengths, a block
   // is either all padding (u > U_b, it ends at once) or all lattice rows
