@@ -22,9 +22,13 @@
 //    the array needs to start at zero: every entry a call reads is written
 //    earlier in the same call, so what the previous call left there is
 //    never used.
-//  - the first call on a device looks up the array's device address
-//    (cudaGetSymbolAddress, with that device current) and caches it; make
-//    that first call before any stream capture.
+//  - the first call in each CUDA context (the first call on a device, and
+//    the first one after cudaDeviceReset or in another context) looks up
+//    the array's device address (cudaGetSymbolAddress, with that context
+//    current) and caches it under the context's unique id; make that first
+//    call before any stream capture.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "../../include/tdt_loss.h"
@@ -40,21 +44,67 @@ constexpr int kMaxDevices = 64;
 // symbol, not a device address: kernels get the address looked up below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_mu;
-void *g_scratch_addr[kMaxDevices] = {};
+// The address is valid only in the context it was looked up in: a device
+// reset (or another context made current on the same device) loads the
+// module again, possibly elsewhere.  So each device's entry remembers the
+// unique id of its context (cuCtxGetId, reached through the runtime's
+// driver entry point, so no link to the driver library is needed).
+struct ScratchEntry {
+  unsigned long long ctx_id = 0;  // 0: no lookup yet
+  void *addr = nullptr;
+};
 
-// Device address of g_noalloc_scratch on the current device (looked up once
-// per device, with that device current).  nullptr on failure.
-void *scratch_on_current_device() {
+std::mutex g_mu;
+ScratchEntry g_scratch[kMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Unique id of the context current on this thread; 0 when none is current
+// or the driver cannot tell.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+    fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(fn);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of g_noalloc_scratch in the current context: cached per
+// device under the context's id, looked up again (with that context
+// current) whenever the id differs.  nullptr on failure.
+void *scratch_in_current_context() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> g(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
-    g_scratch_addr[dev] = ptr;
-  }
-  return g_scratch_addr[dev];
+  unsigned long long id = current_context_id();
+  ScratchEntry &e = g_scratch[dev];
+  if (id != 0 && e.ctx_id == id && e.addr) return e.addr;
+  void *ptr = nullptr;
+  // also makes the device's primary context current if none was
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return nullptr;
+  if (id == 0) id = current_context_id();
+  if (id == 0) return ptr;  // no id to key on: use the fresh address, cache nothing
+  e.ctx_id = id;
+  e.addr = ptr;
+  return ptr;
 }
 
 }  // namespace
@@ -73,7 +123,7 @@ extern "C" int tdt_loss_fwd_bwd_noalloc(const void *logits, const int64_t sizes[
   tdt::Layout L;
   if (!tdt::make_layout(sizes, n_dur, &L)) return TDT_ERR_BAD_SIZES;
   if (L.total > tdt::kNoAllocScratchBytes) return TDT_ERR_NOALLOC_TOO_LARGE;
-  void *scratch = tdt::scratch_on_current_device();
+  void *scratch = tdt::scratch_in_current_context();
   if (!scratch) return TDT_ERR_CUDA;
   const tdt::Workspace ws = tdt::carve(L, scratch);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
