@@ -38,7 +38,7 @@ def _run(binding, inp, compute_grad=True):
 
 @pytest.mark.parametrize("faulted", [0, 2])
 def test_wait_runs_out_and_marks_only_that_utterance(binding, oracle_mod, faulted):
-    w = scaled(WORKLOADS["tiny"], name="halo_fault", B=3, T=40, U=60, V=50, blank=49,
+    w = scaled(WORKLOADS["tiny"], name="halo_fault", B=3, T=40, U=100, V=50, blank=49,
                durations=(0, 1, 2, 3), dtype="f32", std=1.0, sigma=0.05, reduction="none",
                seed=2718)
     inp = make_inputs(w, device="cuda")
