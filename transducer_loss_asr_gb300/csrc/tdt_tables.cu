@@ -22,6 +22,8 @@
 //                            anti-diagonal layout, one contiguous record per
 //                            node for the lattice passes
 // and usable[b] = 1 for every utterance of the launch.
+#include <type_traits>
+
 #include "tdt_rowio.cuh"
 
 namespace tdt {
@@ -86,6 +88,45 @@ __device__ __forceinline__ void group_ms(float &m, float &s, float *sm_m, float 
   }
 }
 
+// Per-row values computed once per row group instead of by every lane:
+// lane 0 of the group takes the token side, lane 1 the duration side, lanes 2
+// and 3 the blank and label logits, and each of the four converts its value(s)
+// to fx in the same two 64-bit conversions (which run on the slow float64
+// pipe); the results are broadcast with shuffles.  Every lane of the warp
+// calls it (inactive rows with neutral inputs), TPR >= 4.
+struct RowScalars {
+  fx_t lse_fx, lsed_fx;  // token and duration log-sum-exps in fx
+  fx_t zb_fx, zy_fx;     // blank and label logits in fx
+  float lse, lsed;       // the same log-sum-exps in fp32 (lane 0 / lane 1)
+};
+
+template <int TPR>
+__device__ __forceinline__ RowScalars row_scalars(int lt, float M, float S, float md, float sd,
+                                                  float zb, float zy, bool has_dur) {
+  // ln(ss) = e ln2 + log1p(f - 1), ss = f 2^e, f in [1, 2): ss >= 1 (the
+  // largest term of a sum taken relative to its maximum is 1)
+  float mm = 0.0f, ss = 1.0f;
+  if (lt == 0) { mm = M; ss = S; }
+  if (lt == 1 && has_dur) { mm = md; ss = sd; }
+  if (!(ss >= 1.0f) || !(mm > -INFINITY)) { mm = 0.0f; ss = 1.0f; }  // inactive rows
+  const int bits = __float_as_int(ss);
+  const int e = ((bits >> 23) & 0xff) - 127;
+  const float f = __int_as_float((bits & 0x007fffff) | 0x3f800000);
+  const float lf = log1pf(f - 1.0f);
+  // the two conversions: lanes 0, 1: (lf, mm); lane 2: zb; lane 3: zy
+  const float a = lt < 2 ? lf : (lt == 2 ? zb : zy);
+  const fx_t v = fx_from_float(a) + (lt < 2 ? fx_from_float(mm) + (fx_t)e * kFxLn2 : (fx_t)0);
+  constexpr int W = TPR < 32 ? TPR : 32;
+  const int base = (threadIdx.x & 31) & ~(W - 1);
+  RowScalars r;
+  r.lse_fx = __shfl_sync(0xffffffffu, v, base);
+  r.lsed_fx = __shfl_sync(0xffffffffu, v, base + 1);
+  r.zb_fx = __shfl_sync(0xffffffffu, v, base + 2);
+  r.zy_fx = __shfl_sync(0xffffffffu, v, base + 3);
+  r.lse = r.lsed = mm + ((float)e * 0.6931471805599453f + lf);
+  return r;
+}
+
 // Outputs of one usable node from its reduced row: the two log-sum-exps
 // and the arc record -- [i] blank arc with duration i, [n_dur + i] label arc
 // with duration i (token log-prob - sigma + duration log-prob).  Lane lt
@@ -93,12 +134,10 @@ __device__ __forceinline__ void group_ms(float &m, float &s, float *sm_m, float 
 template <int TPR, int DPL>
 __device__ __forceinline__ void write_node_outputs(const Problem &p, const Workspace &ws,
                                                    long long n, long long b, long long t,
-                                                   long long u, int lt, float M, float S,
-                                                   float md, float sd, const float *zd, float zb,
-                                                   float zy, bool y_ok) {
-  const fx_t lse_fx = fx_from_float(M) + fx_log_ge1(S);
-  const fx_t wbs = clamp_lp(fx_from_float(zb) - lse_fx) - p.sigma_fx;
-  const fx_t wls = y_ok ? clamp_lp(fx_from_float(zy) - lse_fx) - p.sigma_fx : 0;
+                                                   long long u, int lt, const RowScalars &rs,
+                                                   const float *zd, bool y_ok) {
+  const fx_t wbs = clamp_lp(rs.zb_fx - rs.lse_fx) - p.sigma_fx;
+  const fx_t wls = y_ok ? clamp_lp(rs.zy_fx - rs.lse_fx) - p.sigma_fx : 0;
   fx_t *rec = ws.arcw + diag_index(p, b, t, u) * p.rec_len;
   if (p.rnnt) {
     // plain RNN-T: no duration head; the blank arc advances one frame, the
@@ -108,20 +147,61 @@ __device__ __forceinline__ void write_node_outputs(const Problem &p, const Works
       rec[p.n_dur + lt] = p.dur[lt] == 0 ? wls : kFxVeryNeg;
     }
   } else {
-    const fx_t lsed_fx = fx_from_float(md) + fx_log_ge1(sd);
 #pragma unroll
     for (int c = 0; c < DPL; ++c) {
       const int i = lt + c * TPR;
       if (i < p.D) {
-        const fx_t ld = clamp_lp(fx_from_float(zd[c]) - lsed_fx);
+        const fx_t ld = clamp_lp(fx_from_float(zd[c]) - rs.lsed_fx);
         rec[i] = wbs + ld;
         rec[p.n_dur + i] = wls + ld;
       }
     }
   }
-  if (lt == 0) {
-    ws.lse_tok[n] = M + logf(S);
-    ws.lse_dur[n] = p.D > 0 ? md + logf(sd) : 0.0f;
+  if (lt == 0) ws.lse_tok[n] = rs.lse;
+  if (lt == 1) ws.lse_dur[n] = p.D > 0 ? rs.lsed : 0.0f;
+}
+
+// Largest element of a batch of 16-byte vectors (those with index < nvec):
+// 16-bit types by packed pairwise maxima (one instruction per two elements)
+// before converting, fp32 element by element.
+template <int DT, int KB, int TPR>
+__device__ __forceinline__ float batch_max(const uint4 *v, int j0, int lt, int nvec) {
+  if constexpr (DT == kF32) {
+    float cm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < KB; ++i) {
+      if (j0 + i * TPR + lt < nvec) {
+        cm = fmaxf(cm, fmaxf(fmaxf(__uint_as_float(v[i].x), __uint_as_float(v[i].y)),
+                             fmaxf(__uint_as_float(v[i].z), __uint_as_float(v[i].w))));
+      }
+    }
+    return cm;
+  } else {
+    typedef typename std::conditional<DT == kBF16, __nv_bfloat162, __half2>::type H2;
+    const unsigned neg_inf_pair = DT == kBF16 ? 0xff80ff80u : 0xfc00fc00u;
+    unsigned acc = neg_inf_pair;
+#pragma unroll
+    for (int i = 0; i < KB; ++i) {
+      if (j0 + i * TPR + lt < nvec) {
+        const unsigned w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          H2 a = *reinterpret_cast<const H2 *>(&acc), bb = *reinterpret_cast<const H2 *>(&w[k]);
+          H2 r = __hmax2(a, bb);
+          acc = *reinterpret_cast<const unsigned *>(&r);
+        }
+      }
+    }
+    float x[2];
+    if constexpr (DT == kBF16) {
+      x[0] = __uint_as_float(acc << 16);
+      x[1] = __uint_as_float(acc & 0xffff0000u);
+    } else {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&acc));
+      x[0] = f.x;
+      x[1] = f.y;
+    }
+    return fmaxf(x[0], x[1]);
   }
 }
 
@@ -190,7 +270,7 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
   const bool y_ok = y >= 0 && y < p.V && y != p.blank;
 
   // token logits [0, V)
-  float m = -INFINITY, s = 0.0f;
+  float m = -INFINITY, s = 0.0f, mL = -INFINITY;
   if (active) {
     const uint4 *vbase = reinterpret_cast<const uint4 *>(row + head);
     for (int j0 = 0; j0 < nvec; j0 += TPR * kBatch) {
@@ -202,19 +282,11 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
       }
       // the label's logit, once the label has arrived (overlaps the batch)
       if (j0 == 0 && y_ok) zy = Elem<DT>::load(row + y);
-      float cm = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        if (j0 + i * TPR + lt < nvec) {
-          float x[N];
-          unpack<DT>(v[i], x);
-#pragma unroll
-          for (int e = 0; e < N; ++e) cm = fmaxf(cm, x[e]);
-        }
-      }
+      const float cm = batch_max<DT, kBatch, TPR>(v, j0, lt, nvec);
       if (cm > m) {
         s *= fast_exp2((m - cm) * kLog2e);
         m = cm;
+        mL = m * kLog2e;
       }
       if (m != -INFINITY) {
 #pragma unroll
@@ -222,9 +294,10 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
           if (j0 + i * TPR + lt < nvec) {
             float x[N];
             unpack<DT>(v[i], x);
-            // (x - m) first: exact for the terms near the max, which dominate
+            // x log2(e) - m log2(e) in one rounding; the rounding of m log2(e)
+            // is common to the row's terms (a relative 2^-24 of m log2 e)
 #pragma unroll
-            for (int e = 0; e < N; ++e) s += fast_exp2((x[e] - m) * kLog2e);
+            for (int e = 0; e < N; ++e) s += fast_exp2(fmaf(x[e], kLog2e, -mL));
           }
         }
       }
@@ -244,8 +317,9 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
       if (lt + c * TPR < p.D) merge_ms(md, sd, zd[c], 1.0f);
   }
   group_ms<TPR>(md, sd, sm_m, sm_s);
+  const RowScalars rs = row_scalars<TPR>(lt, M, S, md, sd, zb, zy, p.D > 0);
   if (!active) return;
-  write_node_outputs<TPR, kDurPerLane>(p, ws, n, b, t, u, lt, M, S, md, sd, zd, zb, zy, y_ok);
+  write_node_outputs<TPR, kDurPerLane>(p, ws, n, b, t, u, lt, rs, zd, y_ok);
 }
 
 template <int DT, int TPR>
