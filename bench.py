@@ -515,10 +515,11 @@ def main():
     peak, peak_kind = measured_peaks()
     roofline = None
     ms_g, n_g, span_g = kt.get("grad", (0.0, 0, 0.0))
+    k4_bytes = read_b + write_b
     if n_g and span_g > 0:
         per_step = n_g / args.steps
-        bytes_launch = (read_b + write_b) / per_step
-        achieved = (read_b + write_b) * args.steps / (span_g / 1e3) / 1e9
+        bytes_launch = k4_bytes / per_step
+        achieved = k4_bytes * args.steps / (span_g / 1e3) / 1e9
         tr = NCU_TRAFFIC.get(("grad", w.name))
         traffic = tr["bytes"] if tr and tr["sha256"] == kernel_sha("grad") else None
         roofline = {"bound": "hbm", "kernel": "grad", "achieved": achieved, "peak": peak,
@@ -526,6 +527,7 @@ def main():
                     "algorithmic_bytes_per_launch": bytes_launch,
                     "launches_per_step": per_step,
                     "time": "K4 busy window per step / launches per step",
+                    "bytes_per_step": k4_bytes,
                     "peak_source": peak_kind + " hbm_gbs (copy)"}
     ms_t, n_t, span_t = kt.get("node_tables", (0.0, 0, 0.0))
     if n_t and span_t > 0:
