@@ -194,7 +194,6 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
     const int sh = (int)(first & 15);  // the same for every output vector
     const int qw = sh >> 2, rb = (sh & 3) * 8;
     const uintptr_t abase = first - (uintptr_t)sh;
-    const uintptr_t span = sh ? 32 : 16;
     if (lt < oh) out[lt] = Elem<DT>::from_float(g_at(ld_elem<DT, COH>(row + lt), lt));
     if (lt < p.V - ot0)
       out[ot0 + lt] = Elem<DT>::from_float(g_at(ld_elem<DT, COH>(row + ot0 + lt), ot0 + lt));
@@ -202,28 +201,44 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
     const int jb = (p.blank >= oh && p.blank < ot0) ? (int)((p.blank - oh) / N) : -1;
     const int jy = (y >= oh && y < ot0) ? (int)((y - oh) / N) : -1;
     const int eb = (int)((p.blank - oh) % N), ey = (int)((y - oh) % N);
-    // half the batch: two vectors per output vector in flight
-    constexpr int kFB = kBatch / 2;
+    // One aligned input vector per output vector in flight: the 16 bytes
+    // after it are the next lane's vector, taken by a shuffle; the last lane
+    // of a warp's share of the row (and a lane whose neighbour has no vector)
+    // loads them itself, in the same batch.
+    constexpr int W = TPR < 32 ? TPR : 32;  // lanes of the row group within one warp
+    const bool last_in_warp = (lt % W) == W - 1;
+    constexpr int kFB = 4;
     for (int j0 = 0; j0 < onv; j0 += TPR * kFB) {
       uint4 lo[kFB], hi[kFB];
+      bool lok[kFB], nok[kFB], hok[kFB];
 #pragma unroll
       for (int i = 0; i < kFB; ++i) {
         const int j = j0 + i * TPR + lt;
         const uintptr_t A = abase + 16 * (uintptr_t)j;
-        if (j < onv && A >= rlo && A + span <= rhi) {
-          lo[i] = ld_row16_l1<COH>(reinterpret_cast<const void *>(A));
-          hi[i] = sh ? ld_row16_l1<COH>(reinterpret_cast<const void *>(A + 16)) : lo[i];
+        lok[i] = j < onv && A >= rlo && A + 16 <= rhi;
+        // the neighbour lane's vector is the one at A + 16
+        nok[i] = !last_in_warp && j + 1 < onv && A + 16 >= rlo && A + 32 <= rhi;
+        hok[i] = nok[i];
+        if (lok[i]) lo[i] = ld_row16<COH>(reinterpret_cast<const uint4 *>(A));
+        if (sh && lok[i] && !nok[i] && A + 32 <= rhi) {
+          hi[i] = ld_row16<COH>(reinterpret_cast<const uint4 *>(A + 16));
+          hok[i] = true;
         }
       }
 #pragma unroll
       for (int i = 0; i < kFB; ++i) {
+        uint4 nb;
+        nb.x = __shfl_down_sync(0xffffffffu, lo[i].x, 1);
+        nb.y = __shfl_down_sync(0xffffffffu, lo[i].y, 1);
+        nb.z = __shfl_down_sync(0xffffffffu, lo[i].z, 1);
+        nb.w = __shfl_down_sync(0xffffffffu, lo[i].w, 1);
+        if (nok[i]) hi[i] = nb;
         const int j = j0 + i * TPR + lt;
         if (j < onv) {
-          const uintptr_t A = abase + 16 * (uintptr_t)j;
           const long long k0 = oh + (long long)N * j;
           float x[N];
-          if (A >= rlo && A + span <= rhi) {
-            unpack<DT>(funnel16(lo[i], hi[i], qw, rb), x);
+          if (lok[i] && (sh == 0 || hok[i])) {
+            unpack<DT>(funnel16(lo[i], sh ? hi[i] : lo[i], qw, rb), x);
           } else {
 #pragma unroll
             for (int e = 0; e < N; ++e) x[e] = ld_elem<DT, COH>(row + k0 + e);
