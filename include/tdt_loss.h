@@ -6,8 +6,9 @@
  * #882, list "What's in it"):
  *   - a log-softmax over the vocabulary at every lattice node, and one over
  *     the duration logits;
- *   - alpha/beta passes over the (t,u) lattice with 64-bit accumulation, no
- *     limit of 1024 labels;
+ *   - alpha/beta passes over the (t,u) lattice, no limit of 1024 labels;
+ *     here in the probability domain with an exact int32 exponent beside
+ *     each fp32 mantissa, so no value underflows however long the lattice;
  *   - one fused pass that writes the gradient w.r.t. the token and the
  *     duration logits;
  *   - fp32/fp16/bf16 logits read directly, including a slice

@@ -51,7 +51,7 @@ bool make_layout(const int64_t sizes[4], int n_dur, Layout *L) {
     off = align_up(off + bytes);
     return at;
   };
-  L->arcw = take(ndiag * 8 * (size_t)arc_record_len(n_dur));
+  L->arcw = take(ndiag * sizeof(LV) * (size_t)arc_record_len(n_dur));
   L->alpha = take(ndiag * sizeof(LV));
   L->beta = take(ndiag * sizeof(LV));
   L->lse_tok = take(nodes * 4);
@@ -67,7 +67,7 @@ bool make_layout(const int64_t sizes[4], int n_dur, Layout *L) {
 Workspace carve(const Layout &L, void *base) {
   char *c = static_cast<char *>(base);
   Workspace w;
-  w.arcw = reinterpret_cast<fx_t *>(c + L.arcw);
+  w.arcw = reinterpret_cast<LV *>(c + L.arcw);
   w.alpha = reinterpret_cast<LV *>(c + L.alpha);
   w.beta = reinterpret_cast<LV *>(c + L.beta);
   w.lse_tok = reinterpret_cast<float *>(c + L.lse_tok);

@@ -1,22 +1,26 @@
 // tdt_common.cuh -- definitions shared by the TDT loss kernels (sm_103a).
 //
-// Numeric representation of the lattice.  The per-node arc log-weights are
-// 64-bit fixed point with 32 fraction bits ("fx": value * 2^32, rounded).
-// alpha, beta and the log-likelihood are pairs (m, s) with value
-// m / 2^32 + ln(s): m an exact fx number, s in [1, 2) in fp32 (s = 0 means
-// -inf).  Adding fx values is exact and associative, so the long alpha/beta
-// chains ("float64 accumulation for precision on long label sequences",
-// "tdt-loss: add TDT loss kernel", kernels-community PR #882, "What's in it")
-// carry no rounding in m; per node, the log-sum-exp over its arcs is
-//   M* = max_j (m_j + w_j)                       exact integer max
-//   S  = sum_j s_j * 2^((m_j + w_j - M*) log2 e)  fp32, S in [1, 4D)
-//   (m, s) = (M* + e ln2, S / 2^e)                e = exponent bits of S
-// so the only rounding per node is one fp32 exp and one multiply-add per
-// arc, and no logarithm, 64-bit conversion or division is needed.  GB300
-// runs float64 (and 64-bit int<->float conversions) at a small fraction of
-// its fp32 rate, which is why the arithmetic is integer + fp32 rather than
-// float64.  |m| < 2^62 holds because log-probs are clamped at -4096,
-// |sigma| <= 1024 and T + U + 1 <= 65536.
+// Numeric representation of the lattice.  The node tables first form each
+// arc's log-weight in 64-bit fixed point with 32 fraction bits ("fx": value
+// * 2^32, rounded) from the fp32 logits and log-sum-exps, then store the arc
+// probability as an extended-range float ("xf", struct LV): s * 2^e with an
+// int32 exponent e and an fp32 mantissa s in [1, 2) (s = 0: probability 0).
+// alpha, beta and the likelihood are xf values too, so the recursions run in
+// the probability domain, as sums of products of positive numbers:
+//   e_j = e_src + e_w                       exact integer add
+//   E   = max_j e_j                         exact integer max
+//   S   = sum_j (s_src s_w) 2^(e_j - E)     fp32; the scale is an exact power
+//                                           of two (0 below 2^-126 of the max)
+//   (e, s) = (E + x, S / 2^x)               x = exponent bits of S (exact)
+// The integer exponent carries the range, so nothing underflows however long
+// the chain ("float64 accumulation for precision on long label sequences",
+// "tdt-loss: add TDT loss kernel", kernels-community PR #882, "What's in
+// it"), and the only roundings per node are one fp32 multiply and one add
+// per arc: no exponential, logarithm, conversion or division.  GB300 runs
+// float64 at a small fraction of its fp32 rate, which is why the arithmetic
+// is integer + fp32 rather than float64.  |e| < 2^27 for every non-zero
+// value because log-probs are clamped at -4096, |sigma| <= 1024 and
+// T + U + 1 <= 65536.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -28,14 +32,11 @@ namespace tdt {
 
 typedef long long fx_t;
 
-constexpr int kFracBits = 32;
 constexpr double kFxOne = 4294967296.0;                     // 2^32
-constexpr fx_t kFxNegInf = (fx_t)(-0x7fffffffffffffffLL - 1);  // -inf sentinel
 constexpr float kLogProbFloor = -4096.0f;
 // ln 2 in fx, rounded from the mathematical constant 0.693147180559945309...
 constexpr fx_t kFxLn2 = (fx_t)(0.69314718055994530942 * 4294967296.0 + 0.5);
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kFxToLog2 = (float)(1.4426950408889634 / 4294967296.0);  // fx -> log2 units
 constexpr int kMaxDurations = 32;
 constexpr int kMaxDurationValue = 255;
 
@@ -80,18 +81,20 @@ __host__ __device__ inline int arc_record_len(int n_dur) { return 2 * n_dur; }
 constexpr int kStreamSmemReserve = 32 * 1024;
 constexpr int kLatticeSmemFloor = 200 * 1024;
 
-// A lattice value m / 2^32 + ln(s) (s = 0, m = 0: -inf), 16 bytes so that
-// one aligned load moves both parts.
-struct __align__(16) LV {
-  fx_t m;
+// A lattice value or arc probability s * 2^e (xf), 8 bytes so that one
+// aligned load moves both parts; zero is s = 0, e = kXeZero.
+struct __align__(8) LV {
+  int e;
   float s;
-  float pad;
 };
+// Exponent of a zero value: far below every non-zero value (|e| < 2^27), and
+// two of them added to a third stay in int32.
+constexpr int kXeZero = -(1 << 28);
 
 // Scratch layout (device pointers carved from one workspace block).
 struct Workspace {
   // anti-diagonal-major, node index g = (b * n_diag + t + u) * U1 + u
-  fx_t *arcw;    // [g][rec_len] node arc records (arc_record_len)
+  LV *arcw;      // [g][rec_len] node arc records (arc_record_len): probabilities
   LV *alpha;     // [g]
   LV *beta;      // [g]
   float *frac;   // [g][2 + n_dur]: share of beta(t,u) through its blank arcs,
@@ -164,47 +167,48 @@ __device__ __forceinline__ fx_t fx_from_float(float x) {
   return __float2ll_rn(x * 4294967296.0f);
 }
 
-// fx value of ln(s) for s >= 1, split as e*ln2 + log1p(f - 1), s = f * 2^e,
-// f in [1, 2): the integer part is exact, the rest is one log1pf.
-__device__ __forceinline__ fx_t fx_log_ge1(float s) {
-  int e;
-  float f = frexpf(s, &e);  // s = f * 2^e, f in [0.5, 1)
-  f *= 2.0f;
-  e -= 1;
-  float lf = log1pf(f - 1.0f);
-  return (fx_t)e * kFxLn2 + fx_from_float(lf);
+// ---- extended-range floats (xf) -------------------------------------------
+__device__ __forceinline__ LV xf_zero() {
+  LV v;
+  v.e = kXeZero;
+  v.s = 0.0f;
+  return v;
 }
 
-__device__ __forceinline__ float fx_to_float(fx_t v) { return __ll2float_rn(v) * (1.0f / 4294967296.0f); }
-
-// An fx difference d <= 0 in log2 units, from two 32-bit conversions (the
-// 64-bit one runs at the float64 rate); below -100 (natural) it is -inf.
-__device__ __forceinline__ float fx_diff_log2(fx_t d) {
-  const int hi = (int)(d >> 32);  // floor(d / 2^32)
-  if (hi < -100) return -INFINITY;
-  const unsigned lo = (unsigned)((unsigned long long)d & 0xffffffffull);
-  return fmaf(__uint2float_rn(lo), kFxToLog2, __int2float_rn(hi) * kLog2e);
+// 2^k for k <= 0 as an exact fp32 power of two; 0 below 2^-126.
+__device__ __forceinline__ float pow2_nonpos(int k) {
+  return __int_as_float(max(k + 127, 0) << 23);
 }
 
-// The same with one 32-bit conversion: d rounded to 2^-24 (natural units),
-// which fits 32 bits for d >= -128; below -100 it is -inf.
-__device__ __forceinline__ float fx_diff_log2_fast(fx_t d) {
-  const int hi = (int)(d >> 32);
-  const int v = (int)((d + 128) >> 8);
-  return hi < -100 ? -INFINITY : __int2float_rn(v) * (kLog2e / 16777216.0f);
-}
-
-// Far below any lattice value (|m| < 2^50 for real values) yet safe to add
-// arc weights to: the m of -inf and of missing arcs in the grouped kernel.
-constexpr fx_t kFxVeryNeg = -(1LL << 61);
-
-// (m, s) from an unnormalised sum S >= 1 around the reference M*: pull the
-// exponent bits of S into m (e * ln2, exact in fx), keep the mantissa.
-__device__ __forceinline__ void lv_normalize(float S, fx_t Mstar, fx_t *m, float *s) {
+// The xf value of an unnormalised sum S around the exponent E (S * 2^E):
+// the exponent bits of S move into e, the mantissa stays.  S = 0: zero.
+// Every sum of arc terms taken relative to its largest exponent is >= 1.
+__device__ __forceinline__ LV xf_from_sum(float S, int E) {
+  if (!(S > 0.0f)) return xf_zero();
   const int bits = __float_as_int(S);
-  const int e = (bits >> 23) - 127;
-  *s = __int_as_float((bits & 0x007fffff) | 0x3f800000);
-  *m = Mstar + (fx_t)e * kFxLn2;
+  LV v;
+  v.e = E + ((bits >> 23) - 127);
+  v.s = __int_as_float((bits & 0x007fffff) | 0x3f800000);
+  return v;
+}
+
+// log2(e) * 2^62 rounded to an integer (6653256548922161245.87...).
+constexpr long long kLog2eQ62 = 6653256548922161246LL;
+
+// xf value of exp(w / 2^32) for an fx log-weight w (|w| < 2^62).  The base-2
+// logarithm w log2(e) / 2^32 comes out of one signed 64 x 64-bit high
+// product as fixed point with 30 fraction bits (error < 2^-30): its integer
+// part is the exponent, its fraction goes through exp2f.
+__device__ __forceinline__ LV xf_from_fx(fx_t w) {
+  const long long h = __mul64hi(w, kLog2eQ62);  // floor(log2(p) * 2^30)
+  LV v;
+  v.e = (int)(h >> 30);
+  v.s = exp2f((float)(int)(h & 0x3fffffffLL) * (1.0f / 1073741824.0f));
+  if (v.s >= 2.0f) {  // a fraction within 2^-25 of 1 rounded up
+    v.s *= 0.5f;
+    v.e += 1;
+  }
+  return v;
 }
 
 __device__ __forceinline__ float fast_rcp(float x) {

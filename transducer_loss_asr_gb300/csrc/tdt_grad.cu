@@ -133,11 +133,10 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
     zero_row<DT, TPR>(out, p.VD, lt);
     return;
   }
-  // c_b N with N = exp(alpha + beta - logL) = 2^((m_a + m_b - m_L) log2 e) s_a s_b / s_L
-  // (the fx difference converted with two 32-bit conversions: a 64-bit one
-  // runs at the float64 rate)
-  const float a0 =
-      sc * (fast_exp2(fx_diff_log2(al.m + be.m - ll.m)) * (al.s * be.s / ll.s));
+  // c_b N with the occupancy N = alpha beta / L = 2^k s_a s_b / s_L,
+  // k = e_a + e_b - e_L (N <= 1, so k <= 2): 2^k as an exact fp32 power of two
+  const int k2 = min(max(al.e + be.e - ll.e + 127, 0), 254);
+  const float a0 = sc * (__int_as_float(k2 << 23) * (al.s * be.s / ll.s));
   const float a = a0 * gs, lse2 = lse_t * kLog2e, lsed2 = lse_d * kLog2e;
   const float ab = (a0 * fb) * gs, alb = (a0 * fl) * gs;
   auto g_at = [&](float x, long long k) {

@@ -5,10 +5,11 @@
 // kernel", kernels-community PR #882, "What's in it").  alpha(t,u) depends on
 // (t-d,u) for d > 0 and on (t-d,u-1) for every d including 0, so all of its
 // inputs lie on earlier anti-diagonals t+u: the passes walk the
-// anti-diagonals (in reverse for beta), one barrier per diagonal.  Values
-// are (m, s) pairs (tdt_common.cuh): exact 64-bit fixed point m plus an fp32
-// mantissa s in [1, 2).  alpha and beta are also stored in global memory in
-// the anti-diagonal layout for the gradient pass.
+// anti-diagonals (in reverse for beta), one barrier per diagonal.  Arc
+// weights, alpha and beta are probabilities held as extended-range floats
+// s * 2^e (int32 exponent, fp32 mantissa; tdt_common.cuh), so a node's value
+// is a plain sum of products.  alpha and beta are also stored in global
+// memory in the anti-diagonal layout for the gradient pass.
 //
 // Two variants:
 //  * lattice_cluster_kernel (D <= 9): the rows u of an utterance's lattice
@@ -56,8 +57,6 @@ namespace {
 
 constexpr int kLatticeMaxThreads = 1024;
 
-__device__ __forceinline__ fx_t fmax_fx(fx_t a, fx_t b) { return a > b ? a : b; }
-
 // Block-wide: are the lengths and the used labels of utterance b usable?
 // Also returns sum_b U_b over the batch (for mean_volume).
 __device__ bool check_utterance(const Problem &p, long long b, double *sum_u_out) {
@@ -98,47 +97,29 @@ __device__ void write_utterance_info(const Problem &p, const Workspace &ws, long
   else if (p.reduction == kMeanBatch) c = 1.0 / (double)p.B;
   else if (p.reduction == kMeanVolume) c = 1.0 / sum_u;
   ws.scale[b] = (float)c;
-  if (!ok) {
-    LV z;
-    z.m = 0;
-    z.s = 0.0f;
-    z.pad = 0.0f;
-    ws.loglik[b] = z;
-  }
+  if (!ok) ws.loglik[b] = xf_zero();
 }
 
-// Log-sum-exp of n candidate arcs (M_j, S_j) (S_j = 0: no arc) into (m, s);
-// with term non-null also each arc's unnormalised term and 1 / their sum
-// (n <= 2 * kMaxDurations).
-__device__ void lse_combine_n(const fx_t *M, const float *S, int n, fx_t *m, float *s,
-                              float *term, float *inv_total) {
-  fx_t ms = kFxNegInf;
-  for (int j = 0; j < n; ++j)
-    if (S[j] > 0.0f) ms = fmax_fx(ms, M[j]);
-  if (ms == kFxNegInf) {
-    *m = 0;
-    *s = 0.0f;
-    if (term)
-      for (int j = 0; j < n; ++j) term[j] = 0.0f;
-    if (inv_total) *inv_total = 0.0f;
-    return;
-  }
+// Sum of n candidate arc terms S_j 2^E_j (S_j = 0, E_j = kXeZero: no arc)
+// as an xf value; with term non-null also each term scaled to the largest
+// exponent and 1 / their sum (n <= 2 * kMaxDurations).
+__device__ LV sum_terms_n(const int *E, const float *S, int n, float *term, float *inv_total) {
+  int emax = E[0];
+  for (int j = 1; j < n; ++j) emax = max(emax, E[j]);
   float tot = 0.0f;
   for (int j = 0; j < n; ++j) {
-    float e = 0.0f;
-    if (S[j] > 0.0f) e = S[j] * fast_exp2(fx_diff_log2(M[j] - ms));
-    if (term) term[j] = e;
-    tot += e;
+    const float x = S[j] * pow2_nonpos(E[j] - emax);
+    if (term) term[j] = x;
+    tot += x;
   }
-  lv_normalize(tot, ms, m, s);
-  if (inv_total) *inv_total = fast_rcp(tot);
+  if (inv_total) *inv_total = tot > 0.0f ? fast_rcp(tot) : 0.0f;
+  return xf_from_sum(tot, emax);
 }
 
-__device__ __forceinline__ LV make_lv(fx_t m, float s) {
+__device__ __forceinline__ LV xf_one() {
   LV v;
-  v.m = m;
-  v.s = s;
-  v.pad = 0.0f;
+  v.e = 0;
+  v.s = 1.0f;
   return v;
 }
 
@@ -146,23 +127,19 @@ __device__ __forceinline__ LV make_lv(fx_t m, float s) {
 // Reads alpha and the arc weights from global memory (one thread).
 __device__ void termination(const Problem &p, const Workspace &ws, long long b, long long Tb,
                             long long Ub) {
-  fx_t M[kMaxDurations];
+  int E[kMaxDurations];
   float S[kMaxDurations];
   for (int i = 0; i < p.n_dur; ++i) {
     const int d = p.dur[i];
-    M[i] = 0;
+    E[i] = kXeZero;
     S[i] = 0.0f;
     if (d <= 0 || Tb - d < 0) continue;
     const long long g = diag_index(p, b, Tb - d, Ub);
-    const LV a = ws.alpha[g];
-    const fx_t *rec = ws.arcw + g * p.rec_len;
-    S[i] = a.s;
-    if (a.s > 0.0f) M[i] = a.m + rec[i];
+    const LV a = ws.alpha[g], w = ws.arcw[g * p.rec_len + i];
+    E[i] = a.e + w.e;
+    S[i] = a.s * w.s;
   }
-  fx_t m;
-  float s;
-  lse_combine_n(M, S, p.n_dur, &m, &s, nullptr, nullptr);
-  ws.loglik[b] = make_lv(m, s);
+  ws.loglik[b] = sum_terms_n(E, S, p.n_dur, nullptr, nullptr);
 }
 
 // Shares of beta(t,u) through blank arcs, label arcs and each duration (arc
@@ -197,34 +174,31 @@ alpha_kernel(Problem p, Workspace ws, long long b0) {
     const long long u_hi = s < Ub ? s : Ub;
     for (long long u = u_lo + threadIdx.x; u <= u_hi; u += blockDim.x) {
       const long long t = s - u;
-      fx_t m = 0;
-      float sv = 1.0f;
+      LV v = xf_one();
       if (s > 0) {
-        fx_t M[2 * kMaxDurations];
+        int E[2 * kMaxDurations];
         float S[2 * kMaxDurations];
         for (int i = 0; i < nd; ++i) {
           const int d = p.dur[i];
-          M[i] = M[nd + i] = 0;
+          E[i] = E[nd + i] = kXeZero;
           S[i] = S[nd + i] = 0.0f;
           if (t - d < 0) continue;
           if (d > 0) {
             const long long g = diag_index(p, b, t - d, u);
-            const LV a = ws.alpha[g];
-            const fx_t *rec = ws.arcw + g * p.rec_len;
-            S[i] = a.s;
-            if (a.s > 0.0f) M[i] = a.m + rec[i];
+            const LV a = ws.alpha[g], w = ws.arcw[g * p.rec_len + i];
+            E[i] = a.e + w.e;
+            S[i] = a.s * w.s;
           }
           if (u >= 1) {
             const long long g = diag_index(p, b, t - d, u - 1);
-            const LV a = ws.alpha[g];
-            const fx_t *rec = ws.arcw + g * p.rec_len;
-            S[nd + i] = a.s;
-            if (a.s > 0.0f) M[nd + i] = a.m + rec[nd + i];
+            const LV a = ws.alpha[g], w = ws.arcw[g * p.rec_len + nd + i];
+            E[nd + i] = a.e + w.e;
+            S[nd + i] = a.s * w.s;
           }
         }
-        lse_combine_n(M, S, 2 * nd, &m, &sv, nullptr, nullptr);
+        v = sum_terms_n(E, S, 2 * nd, nullptr, nullptr);
       }
-      ws.alpha[diag_index(p, b, t, u)] = make_lv(m, sv);
+      ws.alpha[diag_index(p, b, t, u)] = v;
     }
     __syncthreads();
   }
@@ -245,34 +219,33 @@ beta_kernel(Problem p, Workspace ws, long long b0) {
     for (long long u = u_lo + threadIdx.x; u <= u_hi; u += blockDim.x) {
       const long long t = s - u;
       const long long q = diag_index(p, b, t, u);
-      const fx_t *rec = ws.arcw + q * p.rec_len;
-      fx_t M[2 * kMaxDurations];
+      const LV *rec = ws.arcw + q * p.rec_len;
+      int E[2 * kMaxDurations];
       float S[2 * kMaxDurations], term[2 * kMaxDurations];
       for (int i = 0; i < nd; ++i) {
         const int d = p.dur[i];
-        M[i] = M[nd + i] = 0;
+        E[i] = E[nd + i] = kXeZero;
         S[i] = S[nd + i] = 0.0f;
         if (d > 0) {
           if (t + d < Tb) {
             const LV bb = ws.beta[diag_index(p, b, t + d, u)];
-            S[i] = bb.s;
-            if (bb.s > 0.0f) M[i] = bb.m + rec[i];
+            E[i] = bb.e + rec[i].e;
+            S[i] = bb.s * rec[i].s;
           } else if (t + d == Tb && u == Ub) {
-            S[i] = 1.0f;
-            M[i] = rec[i];
+            E[i] = rec[i].e;
+            S[i] = rec[i].s;
           }
         }
         if (u < Ub && t + d < Tb) {
           const LV bb = ws.beta[diag_index(p, b, t + d, u + 1)];
-          S[nd + i] = bb.s;
-          if (bb.s > 0.0f) M[nd + i] = bb.m + rec[nd + i];
+          E[nd + i] = bb.e + rec[nd + i].e;
+          S[nd + i] = bb.s * rec[nd + i].s;
         }
       }
-      fx_t m;
-      float sv, inv;
-      lse_combine_n(M, S, 2 * nd, &m, &sv, term, &inv);
+      float inv;
+      const LV v = sum_terms_n(E, S, 2 * nd, term, &inv);
       write_fractions(ws, q, term, inv, nd);
-      ws.beta[q] = make_lv(m, sv);
+      ws.beta[q] = v;
     }
     __syncthreads();
   }
@@ -304,15 +277,14 @@ __device__ __forceinline__ unsigned map_cta(const void *p, unsigned cta) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(cta));
   return r;
 }
-// Asynchronous 16-byte store into another CTA's shared memory that, when the
-// bytes land, counts them on that CTA's mbarrier (complete_tx): no release
-// fence, so the storing thread never waits for its own earlier memory traffic.
+// Asynchronous 8-byte store of a value into another CTA's shared memory
+// that, when the bytes land, counts them on that CTA's mbarrier
+// (complete_tx): no release fence, so the storing thread never waits for its
+// own earlier memory traffic.
 __device__ __forceinline__ void st_async_lv(unsigned addr, const LV &v, unsigned bar_addr) {
-  const unsigned long long m = (unsigned long long)v.m;
   asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];"
-      ::"r"(addr), "r"((unsigned)(m & 0xffffffffull)), "r"((unsigned)(m >> 32)),
-      "r"(__float_as_uint(v.s)), "r"(__float_as_uint(v.pad)), "r"(bar_addr)
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];"
+      ::"r"(addr), "r"((unsigned)v.e), "r"(__float_as_uint(v.s)), "r"(bar_addr)
       : "memory");
 }
 // Arrive on an mbarrier of another CTA of the cluster, relaxed: used only
@@ -352,11 +324,13 @@ template <int REC> struct ClusterRings {
   __device__ __forceinline__ LV &a(int q, int r) const {
     return *reinterpret_cast<LV *>(tdt_dyn_smem + (q & mA) * slotA + r * (int)sizeof(LV));
   }
-  __device__ __forceinline__ const fx_t *w(int q, int r) const {
-    return reinterpret_cast<const fx_t *>(tdt_dyn_smem + offW + (q & mW) * slotW + r * (REC * 8));
+  __device__ __forceinline__ const LV *w(int q, int r) const {
+    return reinterpret_cast<const LV *>(tdt_dyn_smem + offW + (q & mW) * slotW +
+                                        r * (REC * (int)sizeof(LV)));
   }
-  __device__ __forceinline__ fx_t *w_mut(int q, int r) const {
-    return reinterpret_cast<fx_t *>(tdt_dyn_smem + offW + (q & mW) * slotW + r * (REC * 8));
+  __device__ __forceinline__ LV *w_mut(int q, int r) const {
+    return reinterpret_cast<LV *>(tdt_dyn_smem + offW + (q & mW) * slotW +
+                                  r * (REC * (int)sizeof(LV)));
   }
   __device__ __forceinline__ unsigned long long *full(int i) const {
     return reinterpret_cast<unsigned long long *>(tdt_dyn_smem + offBar) + i;
@@ -367,7 +341,8 @@ template <int REC> struct ClusterRings {
 };
 
 size_t cluster_smem_bytes(int RA, int RW, int Rc, int rec) {
-  return (size_t)RA * (Rc + 2) * sizeof(LV) + (size_t)RW * (Rc + 1) * rec * 8 + 2 * (size_t)RA * 8;
+  return (size_t)RA * (Rc + 2) * sizeof(LV) + (size_t)RW * (Rc + 1) * rec * sizeof(LV) +
+         2 * (size_t)RA * 8;
 }
 
 // Copy the arc records of diagonal q for ring rows 0 .. Rc (lattice rows
@@ -378,7 +353,7 @@ size_t cluster_smem_bytes(int RA, int RW, int Rc, int rec) {
 // of that warp commits one group per call, so its group count per step is
 // uniform; the other warps issue no copies.
 template <int REC>
-__device__ __forceinline__ void prefetch_diag(const fx_t *gdiag0, const ClusterRings<REC> &r,
+__device__ __forceinline__ void prefetch_diag(const LV *gdiag0, const ClusterRings<REC> &r,
                                               int q, int u_lo, int Rc, int U1, int Tb, int Ub,
                                               int lane) {
   if (q >= 0 && q < Tb + Ub) {
@@ -388,8 +363,8 @@ __device__ __forceinline__ void prefetch_diag(const fx_t *gdiag0, const ClusterR
     if (u1 > q) u1 = q;
     if (u1 > Ub) u1 = Ub;
     const int nch = u1 >= u0 ? (u1 - u0 + 1) * (REC / 2) : 0;
-    const fx_t *src = gdiag0 + ((long long)q * U1 + u0) * REC;
-    fx_t *dst = r.w_mut(q, u0 - (u_lo - 1));
+    const LV *src = gdiag0 + ((long long)q * U1 + u0) * REC;
+    LV *dst = r.w_mut(q, u0 - (u_lo - 1));
     for (int c = lane; c < nch; c += 32) cp_async16(dst + 2 * c, src + 2 * c);
   }
   cp_async_commit();
@@ -400,56 +375,42 @@ __device__ __forceinline__ void prefetch_diag(const fx_t *gdiag0, const ClusterR
 // lane commits one group per call so the group count per step is uniform.
 // (Measured faster than one copying warp when there is no control warp.)
 template <int REC, int G>
-__device__ __forceinline__ void prefetch_rec(const fx_t *gdiag0, const ClusterRings<REC> &r,
+__device__ __forceinline__ void prefetch_rec(const LV *gdiag0, const ClusterRings<REC> &r,
                                              int q, int u, int ring_row, int k, int Tb, int Ub,
                                              int U1, bool want) {
   const int t = q - u;
   if (want && q >= 0 && u >= 0 && u <= Ub && t >= 0 && t < Tb) {
-    const fx_t *src = gdiag0 + ((long long)q * U1 + u) * REC;
-    fx_t *dst = r.w_mut(q, ring_row);
+    const LV *src = gdiag0 + ((long long)q * U1 + u) * REC;
+    LV *dst = r.w_mut(q, ring_row);
     for (int c = k; c < REC / 2; c += G) cp_async16(dst + 2 * c, src + 2 * c);
   }
   cp_async_commit();
 }
 
-// Group-wide log-sum-exp of this lane's 2J candidates (M_j, S_j).  The
-// reference R is the group's largest integer part, floor(M_j) (the high word
-// of the fx value): a 32-bit max, one shuffle per round, exact, and at most
-// one natural unit below the true maximum, so every term S_j e^(M_j - R) is
-// below 2e and the largest is >= 1.  M_j - R = (hi_j - hmax) + lo_j 2^-32 is
-// converted with the integer difference taken first, so terms near the
-// maximum carry only fp32 rounding of numbers below 1.  Returns R, the sum S
-// (0 when no candidate is finite: the masked ones have S_j = 0) and each
-// candidate's unnormalised term.
+// Group-wide sum of this lane's 2J candidate terms S_j 2^E_j (masked ones:
+// S_j = 0, E_j = kXeZero).  The reference is the group's largest exponent E
+// (a 32-bit max, one shuffle per round), and each term is scaled by the
+// exact power of two 2^(E_j - E), so the largest term keeps its mantissa
+// (>= 1) and no term exceeds 4.  Returns E, the sum S (0 when every
+// candidate is masked) and each candidate's scaled term.
 template <int J, int G>
-__device__ __forceinline__ void group_lse(const fx_t *M, const float *S, fx_t *ref_out,
+__device__ __forceinline__ void group_sum(const int *E, const float *S, int *ref_out,
                                           float *tot_out, float *term) {
-  int hmax = (int)(M[0] >> 32);
+  int emax = E[0];
 #pragma unroll
-  for (int j = 1; j < 2 * J; ++j) hmax = max(hmax, (int)(M[j] >> 32));
+  for (int j = 1; j < 2 * J; ++j) emax = max(emax, E[j]);
 #pragma unroll
-  for (int o = 1; o < G; o <<= 1) hmax = max(hmax, __shfl_xor_sync(0xffffffffu, hmax, o));
+  for (int o = 1; o < G; o <<= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
   float tot = 0.0f;
 #pragma unroll
   for (int j = 0; j < 2 * J; ++j) {
-    const int dh = (int)(M[j] >> 32) - hmax;
-    const unsigned lo = (unsigned)((unsigned long long)M[j] & 0xffffffffull);
-    const float x2 = fmaf(__uint2float_rn(lo), kFxToLog2, (float)dh * kLog2e);
-    term[j] = S[j] * fast_exp2(x2);
+    term[j] = S[j] * pow2_nonpos(E[j] - emax);
     tot += term[j];
   }
 #pragma unroll
   for (int o = 1; o < G; o <<= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-  *ref_out = (fx_t)hmax * (fx_t)4294967296LL;
+  *ref_out = emax;
   *tot_out = tot;
-}
-
-__device__ __forceinline__ LV lv_from_sum(float tot, fx_t ms) {
-  if (!(tot > 0.0f)) return make_lv(kFxVeryNeg, 0.0f);
-  fx_t m;
-  float sv;
-  lv_normalize(tot, ms, &m, &sv);
-  return make_lv(m, sv);
 }
 
 // Per-CTA state shared by the two directions.
@@ -489,7 +450,7 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
   const int u = bd.u_lo + row - 1;
   const bool own = row >= 1 && row <= cp.Rc;
   const bool lower = MULTI && bd.k > 0, upper = MULTI && bd.k + 1 < bd.K;
-  const fx_t *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * REC;
+  const LV *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * REC;
   LV *galpha = ws.alpha + b * p.n_diag * p.U1;
   int di[J], dd[J];
 #pragma unroll
@@ -542,7 +503,7 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     if (MULTI && bd.control_warp) continue;
     const int t = s - u;
     const bool node = own && u <= bd.Ub && t >= 0 && t < bd.Tb;
-    fx_t M[2 * J];
+    int E[2 * J];
     float S[2 * J], term[2 * J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
@@ -550,21 +511,20 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
       const int i = di[j] < ND ? di[j] : 0;
       // blank arc (t-d, u) -> (t, u), d > 0
       const bool okb = node && d > 0 && t - d >= 0;
-      const LV ab = r.a(s - d, rowc);
-      M[2 * j] = okb ? ab.m + r.w(s - d, rowc)[i] : kFxVeryNeg;
-      S[2 * j] = okb ? ab.s : 0.0f;
+      const LV ab = r.a(s - d, rowc), wb = r.w(s - d, rowc)[i];
+      E[2 * j] = okb ? ab.e + wb.e : kXeZero;
+      S[2 * j] = okb ? ab.s * wb.s : 0.0f;
       // label arc (t-d, u-1) -> (t, u), every d
       const bool okl = node && d >= 0 && u >= 1 && t - d >= 0;
-      const LV al = r.a(s - d - 1, rl);
-      M[2 * j + 1] = okl ? al.m + r.w(s - d - 1, rl)[ND + i] : kFxVeryNeg;
-      S[2 * j + 1] = okl ? al.s : 0.0f;
+      const LV al = r.a(s - d - 1, rl), wl = r.w(s - d - 1, rl)[ND + i];
+      E[2 * j + 1] = okl ? al.e + wl.e : kXeZero;
+      S[2 * j + 1] = okl ? al.s * wl.s : 0.0f;
     }
-    fx_t ms;
+    int es;
     float tot;
-    group_lse<J, G>(M, S, &ms, &tot, term);
+    group_sum<J, G>(E, S, &es, &tot, term);
     // every lane of the group holds the node's value; lane 0 stores it
-    const LV v = node ? (s == 0 ? make_lv(0, 1.0f) : lv_from_sum(tot, ms))
-                      : make_lv(kFxVeryNeg, 0.0f);
+    const LV v = node ? (s == 0 ? xf_one() : xf_from_sum(tot, es)) : xf_zero();
     if (own && k == 0) r.a(s, row) = v;
     if (node && k == 0) galpha[(long long)s * bd.U1 + u] = v;
     if (producer) {
@@ -596,7 +556,7 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
   const int u = bd.u_lo + row - 1;
   const bool own = row >= 1 && row <= cp.Rc;
   const bool lower = MULTI && bd.k > 0, upper = MULTI && bd.k + 1 < bd.K;
-  const fx_t *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * REC;
+  const LV *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * REC;
   LV *gbeta = ws.beta + b * p.n_diag * p.U1;
   float *gfrac = ws.frac + b * p.n_diag * p.U1 * (2 + ND);
   int di[J], dd[J];
@@ -649,8 +609,8 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     if (MULTI && bd.control_warp) continue;
     const int t = q - u;
     const bool node = own && u <= bd.Ub && t >= 0 && t < bd.Tb;
-    const fx_t *rec = r.w(q, rowc);
-    fx_t M[2 * J];
+    const LV *rec = r.w(q, rowc);
+    int E[2 * J];
     float S[2 * J], term[2 * J];
 #pragma unroll
     for (int j = 0; j < J; ++j) {
@@ -659,18 +619,18 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
       // blank arc (t, u) -> (t+d, u), d > 0; the final blank lands on T_b
       const bool inb = node && d > 0 && t + d < bd.Tb;
       const bool fin = node && d > 0 && t + d == bd.Tb && u == bd.Ub;
-      const LV bb = r.a(q + d, rowc);
-      M[2 * j] = inb ? bb.m + rec[di_] : (fin ? rec[di_] : kFxVeryNeg);
-      S[2 * j] = inb ? bb.s : (fin ? 1.0f : 0.0f);
+      const LV bb = r.a(q + d, rowc), wb = rec[di_];
+      E[2 * j] = inb ? bb.e + wb.e : (fin ? wb.e : kXeZero);
+      S[2 * j] = inb ? bb.s * wb.s : (fin ? wb.s : 0.0f);
       // label arc (t, u) -> (t+d, u+1)
       const bool okl = node && d >= 0 && u < bd.Ub && t + d < bd.Tb;
-      const LV bl = r.a(q + d + 1, rowc + 1);
-      M[2 * j + 1] = okl ? bl.m + rec[ND + di_] : kFxVeryNeg;
-      S[2 * j + 1] = okl ? bl.s : 0.0f;
+      const LV bl = r.a(q + d + 1, rowc + 1), wl = rec[ND + di_];
+      E[2 * j + 1] = okl ? bl.e + wl.e : kXeZero;
+      S[2 * j + 1] = okl ? bl.s * wl.s : 0.0f;
     }
-    fx_t ms;
+    int es;
     float tot;
-    group_lse<J, G>(M, S, &ms, &tot, term);
+    group_sum<J, G>(E, S, &es, &tot, term);
     const float inv = tot > 0.0f ? fast_rcp(tot) : 0.0f;
     float fb = 0.0f, fl = 0.0f;
     // the node's fraction record; the nodes of a diagonal have adjacent ones
@@ -686,7 +646,7 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
       fb += __shfl_xor_sync(0xffffffffu, fb, o);
       fl += __shfl_xor_sync(0xffffffffu, fl, o);
     }
-    const LV v = node ? lv_from_sum(tot, ms) : make_lv(kFxVeryNeg, 0.0f);
+    const LV v = node ? xf_from_sum(tot, es) : xf_zero();
     if (own && k == 0) r.a(q, row) = v;
     if (node && k == 0) {
       fr[0] = fb * inv;
@@ -964,7 +924,7 @@ __global__ void reduce_kernel(Problem p, Workspace ws, float *loss_out) {
     double L;
     if (!ws.usable[b]) L = __longlong_as_double(0x7ff8000000000000LL);                // NaN
     else if (ws.loglik[b].s == 0.0f) L = __longlong_as_double(0x7ff0000000000000LL);  // +inf
-    else L = -((double)ws.loglik[b].m / kFxOne + log((double)ws.loglik[b].s));
+    else L = -((double)ws.loglik[b].e * 0.69314718055994530942 + log((double)ws.loglik[b].s));
     const double ub = (double)p.label_lens[b];
     if (p.reduction == kNone) loss_out[b] = (float)L;
     acc += (p.reduction == kMean) ? L / ub : L;

@@ -17,8 +17,8 @@
 //
 // Outputs per usable node (t < T_b, u <= U_b):
 //   lse_tok[n], lse_dur[n]   float, for the gradient pass
-//   arcw[g][0..2D)           node arc record in fx (tdt_common.cuh): blank
-//                            and label arc log-weights per duration,
+//   arcw[g][0..2D)           node arc record of xf values (tdt_common.cuh):
+//                            blank and label arc probabilities per duration,
 //                            anti-diagonal layout, one contiguous record per
 //                            node for the lattice passes
 // and usable[b] = 1 for every utterance of the launch.
@@ -129,8 +129,9 @@ __device__ __forceinline__ RowScalars row_scalars(int lt, float M, float S, floa
 
 // Outputs of one usable node from its reduced row: the two log-sum-exps
 // and the arc record -- [i] blank arc with duration i, [n_dur + i] label arc
-// with duration i (token log-prob - sigma + duration log-prob).  Lane lt
-// of the row group holds durations lt, lt + TPR, ... in zd.
+// with duration i, each the arc's probability exp(token log-prob - sigma +
+// duration log-prob) as an xf value, the log-weight summed in fx first.
+// Lane lt of the row group holds durations lt, lt + TPR, ... in zd.
 template <int TPR, int DPL>
 __device__ __forceinline__ void write_node_outputs(const Problem &p, const Workspace &ws,
                                                    long long n, long long b, long long t,
@@ -138,13 +139,13 @@ __device__ __forceinline__ void write_node_outputs(const Problem &p, const Works
                                                    const float *zd, bool y_ok) {
   const fx_t wbs = clamp_lp(rs.zb_fx - rs.lse_fx) - p.sigma_fx;
   const fx_t wls = y_ok ? clamp_lp(rs.zy_fx - rs.lse_fx) - p.sigma_fx : 0;
-  fx_t *rec = ws.arcw + diag_index(p, b, t, u) * p.rec_len;
+  LV *rec = ws.arcw + diag_index(p, b, t, u) * p.rec_len;
   if (p.rnnt) {
     // plain RNN-T: no duration head; the blank arc advances one frame, the
-    // label arc none; the other arcs of the lattice's {0, 1} get no weight
+    // label arc none; the other arcs of the lattice's {0, 1} get probability 0
     if (lt < p.n_dur) {
-      rec[lt] = p.dur[lt] == 1 ? wbs : kFxVeryNeg;
-      rec[p.n_dur + lt] = p.dur[lt] == 0 ? wls : kFxVeryNeg;
+      rec[lt] = p.dur[lt] == 1 ? xf_from_fx(wbs) : xf_zero();
+      rec[p.n_dur + lt] = p.dur[lt] == 0 ? xf_from_fx(wls) : xf_zero();
     }
   } else {
 #pragma unroll
@@ -152,8 +153,8 @@ __device__ __forceinline__ void write_node_outputs(const Problem &p, const Works
       const int i = lt + c * TPR;
       if (i < p.D) {
         const fx_t ld = clamp_lp(fx_from_float(zd[c]) - rs.lsed_fx);
-        rec[i] = wbs + ld;
-        rec[p.n_dur + i] = wls + ld;
+        rec[i] = xf_from_fx(wbs + ld);
+        rec[p.n_dur + i] = xf_from_fx(wls + ld);
       }
     }
   }
