@@ -296,9 +296,14 @@ __device__ __forceinline__ void arrive_cluster_relaxed(unsigned bar_addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_addr)
                : "memory");
 }
-// Lanes per node: one per duration up to 8 (a power of two, so a node's
-// lanes are an aligned part of a warp); 4 lanes of 3 durations for D = 9.
-constexpr int group_lanes(int nd) { return nd <= 1 ? 1 : nd <= 2 ? 2 : nd <= 4 ? 4 : nd <= 8 ? 8 : 4; }
+// Lanes per node: one for up to five durations (a lane takes all 2D arcs of
+// its node), two above (lane k takes durations k, k + 2, ...).  With a term
+// costing an integer add, a multiply and an exact scale, fewer warps per
+// band beat a shorter per-lane chain until a lane holds ~10 terms.  Measured
+// per diagonal, 1 / 2 / 4 / 8 lanes: parakeet (D = 5) 0.475 / 0.531 / 0.577
+// / 0.524 us, large_batch (D = 5) 0.529 / 0.585 / 0.710 / 0.634 us,
+// long_labels (D = 9) 0.915 / 0.853 / 0.893 / 1.058 us.
+constexpr int group_lanes(int nd) { return nd <= 5 ? 1 : 2; }
 
 // Launch-time shape of the cluster variant.
 struct ClusterPlan {
@@ -780,22 +785,22 @@ bool cluster_plan(const Problem &p, int K, ClusterPlan *cp) {
   return false;
 }
 
-// Bands per utterance and direction for a launch of nb utterances.  A
-// diagonal step is bound by issuing the work of all of a CTA's warps, so an
-// utterance whose single band would hold more than 16 warps is split into
-// bands of about 12 warps (measured on large_batch, 121 rows: one band of 31
-// warps 1.16 us per diagonal, three bands of 11 warps 0.93 us with the
-// exchange); parakeet's 11-warp band stays whole (two bands: 40% slower).
-// The bands of a launch take an SM each, so a launch holds at most ~48 of
-// them; the rest of the GPU streams K1/K4.
+// Bands per utterance and direction for a launch of nb utterances.  One
+// band whenever it holds at most 16 warps (splitting parakeet's band in two
+// made it 40% slower: the exchange costs more than the rows it saves).
+// Longer utterances take as many bands as a cluster allows: the step is
+// bound by issuing the work of a CTA's warps, so fewer rows per band are
+// faster (long_labels, 1,201 rows: 16 bands 0.814 us per diagonal, 13 bands
+// 0.853 us; fewer than 13 leave no room for the record ring).  The bands of
+// a launch take an SM each, so a launch holds at most ~48 of them; the rest
+// of the GPU streams K1/K4.
 int preferred_bands(const Problem &p, long long nb) {
   const int forced = g_forced_bands.load();
   if (forced > 0) return forced < kMaxCluster ? forced : kMaxCluster;
   const int warps = (int)(((p.U1 + 1) * group_lanes(p.n_dur) + 31) / 32);
   if (warps <= 16) return 1;
-  int K = (warps + 11) / 12;
   const long long cap = 48 / (2 * (nb > 0 ? nb : 1));
-  if (K > cap) K = cap > 1 ? (int)cap : 1;
+  const int K = cap > 1 ? (int)cap : 1;
   return K < kMaxCluster ? K : kMaxCluster;
 }
 
