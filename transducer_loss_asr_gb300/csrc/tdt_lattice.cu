@@ -56,6 +56,9 @@ std::atomic<long long> g_wait_limit{0};
 namespace {
 
 constexpr int kLatticeMaxThreads = 1024;
+// A single band holds at most 16 warps (more are split into bands), so its
+// kernel may use up to 128 registers per thread.
+constexpr int kLatticeOneBandThreads = 512;
 
 // Block-wide: are the lengths and the used labels of utterance b usable?
 // Also returns sum_b U_b over the batch (for mean_volume).
@@ -457,11 +460,18 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
   const bool lower = MULTI && bd.k > 0, upper = MULTI && bd.k + 1 < bd.K;
   const LV *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * REC;
   LV *galpha = ws.alpha + b * p.n_diag * p.U1;
+  // lane k takes durations k, k + G, ...; with G not dividing ND the last
+  // slot of some lanes is idle; those and the blank arc of duration 0 are
+  // masked by per-lane constants
+  constexpr bool kIdle = (ND % G) != 0;
   int di[J], dd[J];
+  bool live[J], liveb[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) {
-    di[j] = k + G * j;
-    dd[j] = di[j] < ND ? p.dur[di[j]] : -1;
+    live[j] = !kIdle || k + G * j < ND;
+    di[j] = live[j] ? k + G * j : 0;
+    dd[j] = live[j] ? p.dur[di[j]] : 0;
+    liveb[j] = live[j] && dd[j] > 0;  // no blank arc of duration 0
   }
   const int nsteps = bd.Tb + bd.Ub;
   const bool pref = MULTI ? bd.prefetch_warp : row <= cp.Rc;
@@ -510,20 +520,19 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     const bool node = own && u <= bd.Ub && t >= 0 && t < bd.Tb;
     int E[2 * J];
     float S[2 * J], term[2 * J];
+    // blank arc (t-d, u) -> (t, u) and label arc (t-d, u-1) -> (t, u) of
+    // every duration d, with no test per step: a missing source (before frame
+    // 0, below row 0, outside the lattice) reads zero, because the rings
+    // start zeroed and every slot of a non-node holds zero
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-      const int d = dd[j];
-      const int i = di[j] < ND ? di[j] : 0;
-      // blank arc (t-d, u) -> (t, u), d > 0
-      const bool okb = node && d > 0 && t - d >= 0;
+      const int d = dd[j], i = di[j];
       const LV ab = r.a(s - d, rowc), wb = r.w(s - d, rowc)[i];
-      E[2 * j] = okb ? ab.e + wb.e : kXeZero;
-      S[2 * j] = okb ? ab.s * wb.s : 0.0f;
-      // label arc (t-d, u-1) -> (t, u), every d
-      const bool okl = node && d >= 0 && u >= 1 && t - d >= 0;
       const LV al = r.a(s - d - 1, rl), wl = r.w(s - d - 1, rl)[ND + i];
-      E[2 * j + 1] = okl ? al.e + wl.e : kXeZero;
-      S[2 * j + 1] = okl ? al.s * wl.s : 0.0f;
+      E[2 * j] = liveb[j] ? ab.e + wb.e : kXeZero;
+      S[2 * j] = liveb[j] ? ab.s * wb.s : 0.0f;
+      E[2 * j + 1] = live[j] ? al.e + wl.e : kXeZero;
+      S[2 * j + 1] = live[j] ? al.s * wl.s : 0.0f;
     }
     int es;
     float tot;
@@ -564,11 +573,15 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
   const LV *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * REC;
   LV *gbeta = ws.beta + b * p.n_diag * p.U1;
   float *gfrac = ws.frac + b * p.n_diag * p.U1 * (2 + ND);
+  constexpr bool kIdle = (ND % G) != 0;
   int di[J], dd[J];
+  bool live[J], liveb[J];
 #pragma unroll
   for (int j = 0; j < J; ++j) {
-    di[j] = k + G * j;
-    dd[j] = di[j] < ND ? p.dur[di[j]] : -1;
+    live[j] = !kIdle || k + G * j < ND;
+    di[j] = live[j] ? k + G * j : 0;
+    dd[j] = live[j] ? p.dur[di[j]] : 0;
+    liveb[j] = live[j] && dd[j] > 0;  // no blank arc of duration 0
   }
   const int nsteps = bd.Tb + bd.Ub;
   const int last = nsteps - 1;
@@ -584,6 +597,12 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
       prefetch_rec<REC, G>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
     }
   };
+  // the end state (T_b, U_b), one diagonal past the last: value 1
+  if (own && k == 0 && u == bd.Ub) r.a(nsteps, row) = xf_one();
+  // a label arc of duration d from row u lands before T_b on diagonals q < T_b + u - d
+  int lab_end[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) lab_end[j] = bd.Tb + u - dd[j];
   for (int i = 0; i < P; ++i) prefetch(last - i);
   // halo slots armed ahead, as in the alpha pass
   if (MULTI && bd.control && upper)
@@ -617,19 +636,20 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     const LV *rec = r.w(q, rowc);
     int E[2 * J];
     float S[2 * J], term[2 * J];
+    // blank arc (t, u) -> (t+d, u) and label arc (t, u) -> (t+d, u+1) of
+    // every duration d: a missing target (past the last frame, above row U_b,
+    // outside the lattice) reads zero, and the final blank arcs land on the
+    // end state (T_b, U_b), whose slot holds 1.  A label arc must land before
+    // T_b (t + d < T_b, i.e. q < lab_end[j]), which also keeps it off the end
+    // state.
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-      const int d = dd[j];
-      const int di_ = di[j] < ND ? di[j] : 0;
-      // blank arc (t, u) -> (t+d, u), d > 0; the final blank lands on T_b
-      const bool inb = node && d > 0 && t + d < bd.Tb;
-      const bool fin = node && d > 0 && t + d == bd.Tb && u == bd.Ub;
-      const LV bb = r.a(q + d, rowc), wb = rec[di_];
-      E[2 * j] = inb ? bb.e + wb.e : (fin ? wb.e : kXeZero);
-      S[2 * j] = inb ? bb.s * wb.s : (fin ? wb.s : 0.0f);
-      // label arc (t, u) -> (t+d, u+1)
-      const bool okl = node && d >= 0 && u < bd.Ub && t + d < bd.Tb;
-      const LV bl = r.a(q + d + 1, rowc + 1), wl = rec[ND + di_];
+      const int d = dd[j], i = di[j];
+      const LV bb = r.a(q + d, rowc), wb = rec[i];
+      const LV bl = r.a(q + d + 1, rowc + 1), wl = rec[ND + i];
+      const bool okl = live[j] && q < lab_end[j];
+      E[2 * j] = liveb[j] ? bb.e + wb.e : kXeZero;
+      S[2 * j] = liveb[j] ? bb.s * wb.s : 0.0f;
       E[2 * j + 1] = okl ? bl.e + wl.e : kXeZero;
       S[2 * j + 1] = okl ? bl.s * wl.s : 0.0f;
     }
@@ -644,7 +664,7 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     for (int j = 0; j < J; ++j) {
       fb += term[2 * j];
       fl += term[2 * j + 1];
-      if (node && di[j] < ND) fr[2 + di[j]] = (term[2 * j] + term[2 * j + 1]) * inv;
+      if (node && live[j]) fr[2 + di[j]] = (term[2 * j] + term[2 * j + 1]) * inv;
     }
 #pragma unroll
     for (int o = 1; o < G; o <<= 1) {
@@ -680,7 +700,7 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
 // with neighbouring bands, one control warp: it copies the arc records and
 // waits for and releases the halo slots.
 template <int ND, int G, bool MULTI, int P>
-__global__ void __launch_bounds__(kLatticeMaxThreads, 1)
+__global__ void __launch_bounds__(MULTI ? kLatticeMaxThreads : kLatticeOneBandThreads, 1)
 lattice_cluster_kernel(Problem p, Workspace ws, long long b0, ClusterPlan cp) {
   constexpr int REC = 2 * ND;
   __shared__ int s_abort;
@@ -701,6 +721,14 @@ lattice_cluster_kernel(Problem p, Workspace ws, long long b0, ClusterPlan cp) {
   r.offW = (unsigned)(cp.RA * r.slotA);
   r.offBar = r.offW + (unsigned)(cp.RW * r.slotW);
   const int compute_threads = cp.threads - (cp.K > 1 ? 32 : 0);
+  // both rings start as zeros (exponent kXeZero, mantissa 0), so arcs from
+  // or to slots not yet written contribute nothing; every region is a whole
+  // number of 16-byte chunks
+  {
+    const uint4 z = make_uint4((unsigned)kXeZero, 0u, (unsigned)kXeZero, 0u);
+    uint4 *ring = reinterpret_cast<uint4 *>(tdt_dyn_smem);
+    for (unsigned c = threadIdx.x; c < r.offBar / 16; c += blockDim.x) ring[c] = z;
+  }
   if (threadIdx.x == 0) {
     s_abort = 0;
     if (MULTI) {
@@ -762,7 +790,7 @@ bool cluster_plan(const Problem &p, int K, ClusterPlan *cp) {
   const int G = group_lanes(p.n_dur);
   const int Rc = (int)((p.U1 + K - 1) / K);
   const int threads = ((Rc + 1) * G + 31) / 32 * 32 + (K > 1 ? 32 : 0);
-  if (threads > kLatticeMaxThreads) return false;
+  if (threads > (K > 1 ? kLatticeMaxThreads : kLatticeOneBandThreads)) return false;
   const int rec = arc_record_len(p.n_dur);
   // value ring: max_dur + 2 diagonals in use, the rest is how far a band may
   // run ahead of the band it feeds
