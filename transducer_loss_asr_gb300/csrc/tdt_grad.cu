@@ -20,15 +20,23 @@
 // from the lattice pass's outputs together with the row's first batch of
 // logits, so their latencies overlap; every lane of a row group computes
 // them (the loads are broadcasts within a warp).
+#include "tdt_async.cuh"
 #include "tdt_rowio.cuh"
 
 namespace tdt {
+
+extern __shared__ __align__(16) unsigned char tdt_dyn_smem[];
 
 namespace {
 
 constexpr int kGradThreads = 256;
 constexpr int kVecPerThread = 8;      // row vectors per lane when choosing TPR
 constexpr int kLongRowBytes = 16384;  // rows from this size on: one block per row
+constexpr int kStagedTPR = 128;       // realigned long rows staged in shared memory
+
+// 16-byte chunks of one row's staging buffer: the row's token logits plus
+// one chunk at each end for the misalignment.
+__host__ __device__ inline int stage_chunks(long long v_bytes) { return (int)(v_bytes / 16) + 2; }
 
 // 16-byte loads a lane issues before it uses them, and the blocks per SM the
 // registers are sized for.  Measured on GB300: 8 loads for one block per row
@@ -97,6 +105,35 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
   int usable = 0;
   float lse_t = 0.0f, lse_d = 0.0f, fb = 0.0f, fl = 0.0f;
   long long y = -1;
+  // Staged realigned rows (a strided view whose rows sit at another 16-byte
+  // offset than the gradient rows, long rows): the aligned 16-byte chunks of
+  // the row that lie wholly inside its token logits go to the row group's
+  // shared buffer by cp.async before anything else, so no register is held
+  // while they are in flight.  Output vector j (the 16 bytes at `first` +
+  // 16 j of the input) is then chunk j funnel-shifted with chunk j + 1.
+  constexpr bool kStaged = VIEW && TPR == kStagedTPR;
+  int oh = 0, onv = 0, sh = 0, c_lo = 0, c_hi = 0;
+  uintptr_t abase = 0;
+  uint4 *stage = nullptr;
+  if constexpr (kStaged) {
+    if (in_lattice && !vec) {
+      oh = head_elems<DT>(out);
+      if (oh > p.V) oh = (int)p.V;
+      onv = (int)((p.V - oh) / N);
+      const uintptr_t rlo = ai, rhi = ai + (uintptr_t)p.V * sizeof(E);
+      const uintptr_t first = ai + (uintptr_t)oh * sizeof(E);
+      sh = (int)(first & 15);
+      abase = first - (uintptr_t)sh;
+      c_lo = abase >= rlo ? 0 : 1;
+      c_hi = (int)((rhi - abase) / 16);
+      if (c_hi > onv + 1) c_hi = onv + 1;
+      stage = reinterpret_cast<uint4 *>(tdt_dyn_smem) +
+              (threadIdx.x / TPR) * stage_chunks((long long)p.V * sizeof(E));
+      for (int c = c_lo + lt; c < c_hi; c += TPR)
+        cp_async16(stage + c, reinterpret_cast<const void *>(abase + 16 * (uintptr_t)c));
+      cp_async_commit();
+    }
+  }
   if (in_lattice) {
     if (vec) {
 #pragma unroll
@@ -130,6 +167,7 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
   const float gs = gscale ? gscale[p.reduction == kNone ? b : 0] : 1.0f;
   // rows outside a usable lattice, or of zero occupancy, get a zero gradient
   if (!in_lattice || !usable || al.s == 0.0f || be.s == 0.0f || ll.s == 0.0f) {
+    if constexpr (kStaged) cp_async_wait<0>();  // no copy outlives its thread
     zero_row<DT, TPR>(out, p.VD, lt);
     return;
   }
@@ -175,6 +213,41 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
           vout[j] = pack<DT>(x);
         }
       }
+    }
+  } else if constexpr (kStaged) {
+    const long long ot0 = oh + (long long)onv * N;
+    if (lt < oh) out[lt] = Elem<DT>::from_float(g_at(ld_elem<DT, COH>(row + lt), lt));
+    if (lt < p.V - ot0)
+      out[ot0 + lt] = Elem<DT>::from_float(g_at(ld_elem<DT, COH>(row + ot0 + lt), ot0 + lt));
+    uint4 *vout = reinterpret_cast<uint4 *>(out + oh);
+    const int jb = (p.blank >= oh && p.blank < ot0) ? (int)((p.blank - oh) / N) : -1;
+    const int jy = (y >= oh && y < ot0) ? (int)((y - oh) / N) : -1;
+    const int eb = (int)((p.blank - oh) % N), ey = (int)((y - oh) % N);
+    const int qw = sh >> 2, rb = (sh & 3) * 8;
+    // every chunk of the row group has landed: own copies, then the group's
+    // named barrier (ids 1, 2, ...: one per row group of the block)
+    cp_async_wait<0>();
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + (int)threadIdx.x / TPR), "r"(TPR) : "memory");
+    for (int j = lt; j < onv; j += TPR) {
+      float x[N];
+      if (j >= c_lo && j + (sh ? 1 : 0) < c_hi) {
+        const uint4 lo = stage[j];
+        unpack<DT>(sh ? funnel16(lo, stage[j + 1], qw, rb) : lo, x);
+      } else {  // a vector whose input span leaves the row: element loads
+        const long long k0 = oh + (long long)N * j;
+#pragma unroll
+        for (int e = 0; e < N; ++e) x[e] = ld_elem<DT, COH>(row + k0 + e);
+      }
+      // the blank and label entries by unrolled compares (a runtime index
+      // into x would put it in local memory)
+      const int kb = j == jb ? eb : -1, ky = j == jy ? ey : -1;
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        x[e] = a * fast_exp2(fmaf(x[e], kLog2e, -lse2));
+        if (e == kb) x[e] -= ab;
+        if (e == ky) x[e] -= alb;
+      }
+      vout[j] = pack<DT>(x);
     }
   } else if constexpr (VIEW) {
     // The input and output rows sit at different offsets from a 16-byte
@@ -283,8 +356,19 @@ cudaError_t launch_tpr(const Problem &p, const Workspace &ws, typename Elem<DT>:
   auto kern = overlap       ? grad_kernel<DT, TPR, true, false>
               : same_layout ? grad_kernel<DT, TPR, false, false>
                             : grad_kernel<DT, TPR, false, true>;
-  kern<<<(unsigned)blocks, kGradThreads, kStreamSmemReserve, stream>>>(p, ws, grad, gscale,
-                                                                       n_begin, n_end);
+  // the staged realigned rows keep their chunks in the dynamic shared memory
+  // (the streaming passes request at least kStreamSmemReserve anyway)
+  size_t smem = kStreamSmemReserve;
+  if (TPR == kStagedTPR && !overlap && !same_layout) {
+    const size_t st = (size_t)RPB * 16 * stage_chunks(p.V * (long long)sizeof(*grad));
+    if (st > smem) smem = st;
+    if (smem > 48 * 1024) {
+      const cudaError_t e =
+          cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  kern<<<(unsigned)blocks, kGradThreads, smem, stream>>>(p, ws, grad, gscale, n_begin, n_end);
   return cudaGetLastError();
 }
 
