@@ -32,7 +32,6 @@ namespace {
 constexpr int kGradThreads = 256;
 constexpr int kVecPerThread = 8;      // row vectors per lane when choosing TPR
 constexpr int kLongRowBytes = 16384;  // rows from this size on: one block per row
-constexpr int kStagedTPR = 128;       // realigned long rows staged in shared memory
 
 // 16-byte chunks of one row's staging buffer: the row's token logits plus
 // one chunk at each end for the misalignment.
@@ -64,8 +63,10 @@ __device__ __forceinline__ void zero_row(typename Elem<DT>::T *out, long long VD
 
 // VIEW: the logits rows may sit at another offset from a 16-byte boundary
 // than the gradient rows (a strided view); without it every row is known to
-// share the gradient row's alignment (one contiguous layout).
-template <int DT, int TPR, bool COH, bool VIEW>
+// share the gradient row's alignment (one contiguous layout).  STAGE: the
+// row's 16-byte chunks go to shared memory by cp.async (see below) instead
+// of being loaded into registers in batches.
+template <int DT, int TPR, bool COH, bool VIEW, bool STAGE>
 __global__ void __launch_bounds__(kGradThreads, GradShape<TPR>::kMinBlocks)
 grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gscale,
             long long n_begin, long long n_end) {
@@ -105,18 +106,28 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
   int usable = 0;
   float lse_t = 0.0f, lse_d = 0.0f, fb = 0.0f, fl = 0.0f;
   long long y = -1;
-  // Staged realigned rows (a strided view whose rows sit at another 16-byte
-  // offset than the gradient rows, long rows): the aligned 16-byte chunks of
-  // the row that lie wholly inside its token logits go to the row group's
-  // shared buffer by cp.async before anything else, so no register is held
-  // while they are in flight.  Output vector j (the 16 bytes at `first` +
-  // 16 j of the input) is then chunk j funnel-shifted with chunk j + 1.
-  constexpr bool kStaged = VIEW && TPR == kStagedTPR;
+  // Staged rows: the aligned 16-byte chunks of the row that lie wholly
+  // inside its token logits go to the row group's shared buffer by cp.async
+  // before anything else, so no register is held while they are in flight.
+  // A row at the gradient row's 16-byte offset takes chunk j for output
+  // vector j, each lane reading back only the chunks it copied.  A realigned
+  // row (a strided view at another offset) takes for output vector j (the
+  // 16 bytes at `first` + 16 j of the input) chunk j funnel-shifted with
+  // chunk j + 1, copied by the next lane.
+  // (a strided view stages only its realigned rows: the few rows that meet
+  // the gradient's offset keep the register batches)
+  constexpr bool kStaged = STAGE;
+  constexpr bool kStagedAligned = STAGE && !VIEW;
   int oh = 0, onv = 0, sh = 0, c_lo = 0, c_hi = 0;
   uintptr_t abase = 0;
   uint4 *stage = nullptr;
   if constexpr (kStaged) {
-    if (in_lattice && !vec) {
+    stage = reinterpret_cast<uint4 *>(tdt_dyn_smem) +
+            (threadIdx.x / TPR) * stage_chunks((long long)p.V * sizeof(E));
+    if (kStagedAligned && in_lattice && vec) {
+      for (int c = lt; c < nvec; c += TPR) cp_async16(stage + c, vin + c);
+      cp_async_commit();
+    } else if (VIEW && in_lattice && !vec) {
       oh = head_elems<DT>(out);
       if (oh > p.V) oh = (int)p.V;
       onv = (int)((p.V - oh) / N);
@@ -127,8 +138,6 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
       c_lo = abase >= rlo ? 0 : 1;
       c_hi = (int)((rhi - abase) / 16);
       if (c_hi > onv + 1) c_hi = onv + 1;
-      stage = reinterpret_cast<uint4 *>(tdt_dyn_smem) +
-              (threadIdx.x / TPR) * stage_chunks((long long)p.V * sizeof(E));
       for (int c = c_lo + lt; c < c_hi; c += TPR)
         cp_async16(stage + c, reinterpret_cast<const void *>(abase + 16 * (uintptr_t)c));
       cp_async_commit();
@@ -136,10 +145,12 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
   }
   if (in_lattice) {
     if (vec) {
+      if constexpr (!kStagedAligned) {
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int j = i * TPR + lt;
-        if (j < nvec) v[i] = ld_row16<COH>(vin + j);
+        for (int i = 0; i < kBatch; ++i) {
+          const int j = i * TPR + lt;
+          if (j < nvec) v[i] = ld_row16<COH>(vin + j);
+        }
       }
       if (lt < head) zh = ld_elem<DT, COH>(row + lt);
       if (lt < ntail) zt = ld_elem<DT, COH>(row + tail0 + lt);
@@ -192,6 +203,21 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
     const int jb = (p.blank >= head && p.blank < tail0) ? (int)((p.blank - head) / N) : -1;
     const int jy = (y >= head && y < tail0) ? (int)((y - head) / N) : -1;
     const int eb = (int)((p.blank - head) % N), ey = (int)((y - head) % N);
+    if constexpr (kStagedAligned) {
+      cp_async_wait<0>();  // the lane's own chunks, the only ones it reads
+      for (int j = lt; j < nvec; j += TPR) {
+        float x[N];
+        unpack<DT>(stage[j], x);
+        const int kb = j == jb ? eb : -1, ky = j == jy ? ey : -1;
+#pragma unroll
+        for (int e = 0; e < N; ++e) {
+          x[e] = a * fast_exp2(fmaf(x[e], kLog2e, -lse2));
+          if (e == kb) x[e] -= ab;
+          if (e == ky) x[e] -= alb;
+        }
+        vout[j] = pack<DT>(x);
+      }
+    } else {
     for (int j0 = 0; j0 < nvec; j0 += TPR * kBatch) {
       if (j0 > 0) {
 #pragma unroll
@@ -214,7 +240,8 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
         }
       }
     }
-  } else if constexpr (kStaged) {
+    }
+  } else if constexpr (kStaged && VIEW) {
     const long long ot0 = oh + (long long)onv * N;
     if (lt < oh) out[lt] = Elem<DT>::from_float(g_at(ld_elem<DT, COH>(row + lt), lt));
     if (lt < p.V - ot0)
@@ -227,7 +254,12 @@ grad_kernel(Problem p, Workspace ws, typename Elem<DT>::T *grad, const float *gs
     // every chunk of the row group has landed: own copies, then the group's
     // named barrier (ids 1, 2, ...: one per row group of the block)
     cp_async_wait<0>();
-    asm volatile("bar.sync %0, %1;" ::"r"(1 + (int)threadIdx.x / TPR), "r"(TPR) : "memory");
+    if constexpr (TPR >= 32) {
+      asm volatile("bar.sync %0, %1;" ::"r"(1 + (int)threadIdx.x / TPR), "r"(TPR) : "memory");
+    } else {
+      const unsigned lane = threadIdx.x & 31;
+      __syncwarp(((1u << TPR) - 1u) << (lane & ~(unsigned)(TPR - 1)));
+    }
     for (int j = lt; j < onv; j += TPR) {
       float x[N];
       if (j >= c_lo && j + (sh ? 1 : 0) < c_hi) {
@@ -353,13 +385,21 @@ cudaError_t launch_tpr(const Problem &p, const Workspace &ws, typename Elem<DT>:
                             15) == 0;
   // (an output that overlaps the logits is the contiguous logits themselves:
   // the argument checks reject any other overlap)
-  auto kern = overlap       ? grad_kernel<DT, TPR, true, false>
-              : same_layout ? grad_kernel<DT, TPR, false, false>
-                            : grad_kernel<DT, TPR, false, true>;
-  // the staged realigned rows keep their chunks in the dynamic shared memory
-  // (the streaming passes request at least kStreamSmemReserve anyway)
+  // staged rows (chunks to shared memory by cp.async): realigned long rows
+  // of a strided view, and fp32 rows of one contiguous layout; never when
+  // writing in place.  Measured per step: parakeet 0.4995 vs 0.5096 ms,
+  // long_labels 3.485 vs 3.519 ms; contiguous bf16 rows were slower staged
+  // (large_batch 1.576 vs 1.519 ms) and keep the register batches.
+  const bool stage = !overlap && (same_layout ? DT == kF32 : TPR == 128);
+  auto kern = overlap       ? grad_kernel<DT, TPR, true, false, false>
+              : same_layout ? (stage ? grad_kernel<DT, TPR, false, false, true>
+                                     : grad_kernel<DT, TPR, false, false, false>)
+                            : (stage ? grad_kernel<DT, TPR, false, true, true>
+                                     : grad_kernel<DT, TPR, false, true, false>);
+  // staged rows keep their chunks in the dynamic shared memory (the
+  // streaming passes request at least kStreamSmemReserve anyway)
   size_t smem = kStreamSmemReserve;
-  if (TPR == kStagedTPR && !overlap && !same_layout) {
+  if (stage) {
     const size_t st = (size_t)RPB * 16 * stage_chunks(p.V * (long long)sizeof(*grad));
     if (st > smem) smem = st;
     if (smem > 48 * 1024) {
