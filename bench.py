@@ -49,12 +49,13 @@ FALLBACK_HBM_GBS = 6800.0
 # capture (dram__bytes_read.sum + dram__bytes_write.sum), valid only while
 # its sources hash to this sha256 (kernel_sha).
 NCU_TRAFFIC = {
-    # ncu --set full, one launch = one utterance [1,200,41,8198] fp32 (the
-    # per-launch work of the four-chunk B=4 bench): read 269788160 + written
-    # 209614336 bytes (the rest of the writes retire from L2 after the kernel)
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum, one launch =
+    # one utterance [1,200,41,8198] fp32 (the per-launch work of the
+    # four-chunk B=4 bench): read 269423872 + written 213804288 bytes (the
+    # rest of the writes retire from L2 after the kernel)
     ("grad", "parakeet"): {
-        "bytes": 269788160 + 209614336,
-        "sha256": "c2576d921a4875591be1f59d51ad7d2b9da5830f3f6ebee656cb8242dd457342",
+        "bytes": 269423872 + 213804288,
+        "sha256": "d21c9200aaec253f1bf6381f986f5a25aab2098c8c24b7357c677aa0ded33814",
     },
 }
 
@@ -165,7 +166,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-KERNEL_SOURCES = {"grad": ("tdt_grad.cu", "tdt_rowio.cuh", "tdt_common.cuh")}
+KERNEL_SOURCES = {"grad": ("tdt_grad.cu", "tdt_rowio.cuh", "tdt_async.cuh", "tdt_common.cuh")}
 
 
 def kernel_sha(kernel):
