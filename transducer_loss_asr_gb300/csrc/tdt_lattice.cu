@@ -14,16 +14,17 @@
 // Two variants:
 //  * lattice_cluster_kernel (D <= 9): the rows u of an utterance's lattice
 //    are split into K bands, one CTA each, the K CTAs of an utterance and
-//    direction forming a thread-block cluster.  G lanes serve one node (lane
-//    k takes durations k, k+G, ...).  A CTA keeps the values of the last RA
+//    direction forming a thread-block cluster.  G lanes serve one node (one
+//    up to five durations, else two; lane k takes durations k, k+G, ...).
+//    A CTA keeps the values of the last RA
 //    diagonals of its rows in a shared ring, and the arc records of the
 //    diagonals in flight in a second ring filled with cp.async P diagonals
 //    ahead (with several bands by the control warp, a diagonal's records of
 //    the band's rows being one contiguous block in the anti-diagonal layout;
 //    with one band by each node's lanes), so no global round trip sits on
 //    the diagonal-to-diagonal path.  K: one band up to 16 compute warps,
-//    else bands of ~12 warps (then the fewest whose rings fit).  With K = 1
-//    the kernel is compiled without any exchange.
+//    else as many bands as a cluster allows (then the fewest whose rings
+//    fit).  With K = 1 the kernel is compiled without any exchange.
 //    With K > 1 the one row a band needs from its neighbour (u_lo - 1 for
 //    alpha, u_hi + 1 for beta) is pushed into the neighbour's ring through
 //    distributed shared memory after every diagonal (st.async counted on an
