@@ -32,6 +32,7 @@ namespace {
 constexpr int kGradThreads = 256;
 constexpr int kVecPerThread = 8;      // row vectors per lane when choosing TPR
 constexpr int kLongRowBytes = 16384;  // rows from this size on: one block per row
+constexpr int kStagedViewTPR = 64;    // lanes per realigned long row (staged)
 
 // 16-byte chunks of one row's staging buffer: the row's token logits plus
 // one chunk at each end for the misalignment.
@@ -390,7 +391,7 @@ cudaError_t launch_tpr(const Problem &p, const Workspace &ws, typename Elem<DT>:
   // writing in place.  Measured per step: parakeet 0.4995 vs 0.5096 ms,
   // long_labels 3.485 vs 3.519 ms; contiguous bf16 rows were slower staged
   // (large_batch 1.576 vs 1.519 ms) and keep the register batches.
-  const bool stage = !overlap && (same_layout ? DT == kF32 : TPR == 128);
+  const bool stage = !overlap && (same_layout ? DT == kF32 : TPR == kStagedViewTPR);
   auto kern = overlap       ? grad_kernel<DT, TPR, true, false, false>
               : same_layout ? (stage ? grad_kernel<DT, TPR, false, false, true>
                                      : grad_kernel<DT, TPR, false, false, false>)
@@ -421,15 +422,16 @@ cudaError_t launch_dt(const Problem &p, const Workspace &ws, void *grad_out, con
   int tpr =
       row_bytes >= kLongRowBytes ? 256 : row_group_threads(row_bytes, kVecPerThread);
   // Long rows of a strided view whose rows sit at other 16-byte offsets than
-  // the gradient rows (the realigned path): 128 lanes per row, two rows per
-  // block (measured on the bf16 [..., :8198] view of [..., 8205], ragged:
-  // 0.334 vs 0.346 ms per step with 256 lanes; 64 lanes 0.335, 32 lanes 0.352)
+  // the gradient rows (the staged realigned path): 64 lanes per row, four
+  // rows per block (measured on the bf16 [..., :8198] view of [..., 8205],
+  // ragged: 0.2585-0.2592 ms per step, against 0.263 with 128 lanes and
+  // 0.291 with 256)
   if (tpr == 256) {
     const char *lo = static_cast<const char *>(p.logits);
     const bool same_layout =
         p.s2 == p.VD && p.s1 == p.U1 * p.VD && p.s0 == p.T * p.s1 &&
         ((reinterpret_cast<uintptr_t>(lo) - reinterpret_cast<uintptr_t>(g)) & 15) == 0;
-    if (!same_layout) tpr = 128;
+    if (!same_layout) tpr = kStagedViewTPR;
   }
   switch (tpr) {
     case 8: return launch_tpr<DT, 8>(p, ws, g, gscale, n_begin, n_end, stream);
