@@ -206,13 +206,13 @@ __device__ __forceinline__ float batch_max(const uint4 *v, int j0, int lt, int n
   }
 }
 
-template <int DT, int TPR>
+template <int DT, int TPR, int DPL>
 __global__ void __launch_bounds__(kTablesThreads, 4)
 node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) {
   typedef typename Elem<DT>::T E;
   constexpr int N = Vec<DT>::N;
   constexpr int RPB = kTablesThreads / TPR;
-  constexpr int kDurPerLane = (kMaxDurations + TPR - 1) / TPR;  // D <= kMaxDurations
+  constexpr int kDurPerLane = DPL;  // duration logits a lane holds (D <= TPR * DPL)
   __shared__ float sm_m[kTablesThreads / 32], sm_s[kTablesThreads / 32];
   const E *logits = static_cast<const E *>(p.logits);
   const int lt = threadIdx.x % TPR;
@@ -323,15 +323,30 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
   write_node_outputs<TPR, kDurPerLane>(p, ws, n, b, t, u, lt, rs, zd, y_ok);
 }
 
-template <int DT, int TPR>
-cudaError_t launch_tpr(const Problem &p, const Workspace &ws, long long n_begin, long long n_end,
-                       cudaStream_t stream) {
+template <int DT, int TPR, int DPL>
+cudaError_t launch_tpr_dpl(const Problem &p, const Workspace &ws, long long n_begin,
+                           long long n_end, cudaStream_t stream) {
   constexpr int RPB = kTablesThreads / TPR;
   const long long rows = n_end - n_begin;
   const long long blocks = (rows + RPB - 1) / RPB;
-  node_tables_kernel<DT, TPR><<<(unsigned)blocks, kTablesThreads, kStreamSmemReserve, stream>>>(
-      p, ws, n_begin, n_end);
+  node_tables_kernel<DT, TPR, DPL>
+      <<<(unsigned)blocks, kTablesThreads, kStreamSmemReserve, stream>>>(p, ws, n_begin, n_end);
   return cudaGetLastError();
+}
+
+// Duration logits per lane: the fewest (1, 2 or 4, else all that D may
+// need) that hold the problem's D.
+template <int DT, int TPR>
+cudaError_t launch_tpr(const Problem &p, const Workspace &ws, long long n_begin, long long n_end,
+                       cudaStream_t stream) {
+  constexpr int kFull = (kMaxDurations + TPR - 1) / TPR;
+  const long long need = (p.D + TPR - 1) / TPR;
+  if (need <= 1) return launch_tpr_dpl<DT, TPR, 1>(p, ws, n_begin, n_end, stream);
+  if constexpr (kFull >= 2)
+    if (need <= 2) return launch_tpr_dpl<DT, TPR, 2>(p, ws, n_begin, n_end, stream);
+  if constexpr (kFull >= 4)
+    if (need <= 4) return launch_tpr_dpl<DT, TPR, 4>(p, ws, n_begin, n_end, stream);
+  return launch_tpr_dpl<DT, TPR, kFull>(p, ws, n_begin, n_end, stream);
 }
 
 template <int DT>
