@@ -155,6 +155,8 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
   p->n_diag = T + U1 - 1;
   p->rec_len = arc_record_len(n_dur);
   p->rnnt = rnnt ? 1 : 0;
+  fast_div_setup(T, &p->divT_m, &p->divT_s);
+  fast_div_setup(U1, &p->divU1_m, &p->divU1_s);
   return TDT_OK;
 }
 

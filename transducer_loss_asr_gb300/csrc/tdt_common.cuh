@@ -66,7 +66,24 @@ struct Problem {
                                   //    before it gives up (set by launch_lattice)
   long long fault_utt;            // testing: the utterance whose band 1 never publishes
                                   //    its boundary row (-1: none; set by launch_lattice)
+  unsigned divT_m, divU1_m;       // n / T and n / U1 for n < 2^31 as (n m) >> s
+  int divT_s, divU1_s;            //    (set by the host, fast_div_setup)
 };
+
+// Division of n < 2^31 by an invariant d >= 1 with one 32 x 32 -> 64-bit
+// multiply and a shift: with l = ceil(log2 d), m = floor(2^(31+l) / d) + 1
+// (< 2^32) and s = 31 + l, floor(n / d) = (n m) >> s for every n < 2^31
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994).
+inline void fast_div_setup(long long d, unsigned *m, int *s) {
+  int l = 0;
+  while ((1LL << l) < d) ++l;
+  *s = 31 + l;
+  *m = (unsigned)(((unsigned long long)1 << *s) / (unsigned long long)d + 1ull);
+}
+__device__ __forceinline__ unsigned fast_div(unsigned n, unsigned m, int s) {
+  return (unsigned)(((unsigned long long)n * m) >> s);
+}
 
 // Node arc record (fx values), one per lattice node in anti-diagonal order:
 //   [i] = lpB - sigma + lpD_i      blank arc with duration i
@@ -121,9 +138,9 @@ __host__ __device__ inline long long diag_index(const Problem &p, long long b, l
 __device__ __forceinline__ void decode_node(const Problem &p, long long n, long long *b,
                                             long long *t, long long *u) {
   const unsigned nn = (unsigned)n, U1 = (unsigned)p.U1, T = (unsigned)p.T;
-  const unsigned bt = nn / U1;
+  const unsigned bt = fast_div(nn, p.divU1_m, p.divU1_s);
   *u = nn - bt * U1;
-  const unsigned bb = bt / T;
+  const unsigned bb = fast_div(bt, p.divT_m, p.divT_s);
   *t = bt - bb * T;
   *b = bb;
 }

@@ -40,9 +40,9 @@ constexpr int kVecPerThread = 16;  // row vectors per thread when choosing TPR
 __device__ __forceinline__ void decode_slot_umajor(const Problem &p, long long k, long long *b,
                                                    long long *t, long long *u) {
   const unsigned kk = (unsigned)k, U1 = (unsigned)p.U1, T = (unsigned)p.T;
-  const unsigned bu = kk / T;
+  const unsigned bu = fast_div(kk, p.divT_m, p.divT_s);
   *t = kk - bu * T;
-  const unsigned bb = bu / U1;
+  const unsigned bb = fast_div(bu, p.divU1_m, p.divU1_s);
   *u = bu - bb * U1;
   *b = bb;
 }
