@@ -331,6 +331,9 @@ def main():
     ap.add_argument("--max-symbols", type=int, default=10)
     ap.add_argument("--lattice-bands", type=int, default=0,
                     help="force K row bands per utterance in the lattice passes (0: automatic)")
+    ap.add_argument("--lattice-exchange", type=int, default=0,
+                    help="how lattice bands exchange boundary rows: 0 automatic, "
+                         "1 thread-block cluster, 2 global memory (tuning)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -364,6 +367,7 @@ def main():
     from transducer_loss_asr_gb300 import binding
 
     binding.tdt_loss_set_lattice_bands(args.lattice_bands)
+    binding.tdt_loss_set_lattice_exchange(args.lattice_exchange)
     inp = make_inputs(w, device=dev, seed=w.seed + rank)
     if args.op == "decode":
         return run_decode(args, w, inp, dev, world, rank, dist)

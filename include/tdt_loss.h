@@ -276,13 +276,25 @@ int tdt_loss_timing_read(double *ms_out, int64_t *count_out, double *span_ms_out
 
 /*
  * Tuning and testing support.  The lattice passes split an utterance's rows
- * u into K bands, one CTA each, in a thread-block cluster (K <= 16).
- * bands > 0 forces K = min(bands, 16) for later calls (fewer when such a
- * cluster does not fit the GPU); 0 restores the per-problem choice.  The
- * results do not depend on K, bit for bit.  Process-wide; returns the
- * previous setting.
+ * u into K bands, one CTA each.  The bands exchange their boundary rows
+ * either inside a thread-block cluster (K <= 16; distributed shared memory)
+ * or through global memory (any K; each band polls its neighbour's boundary
+ * row in L2).  bands > 0 forces K for later calls: up to 16 in a cluster
+ * (fewer when such a cluster does not fit the GPU) unless global exchange is
+ * forced, above 16 through global memory; 0 restores the per-problem choice.
+ * The results do not depend on K or on the exchange, bit for bit.
+ * Process-wide; returns the previous setting.
  */
 int tdt_loss_set_lattice_bands(int bands);
+
+/*
+ * Tuning and testing support: how lattice bands exchange boundary rows for
+ * later calls.  mode 0: chosen per problem (global memory for lattices too
+ * tall for one CTA; a cluster for forced counts up to 16), 1: always a
+ * cluster (at most 16 bands), 2: always global memory.  Other values act as
+ * 0.  Process-wide; returns the previous setting.
+ */
+int tdt_loss_set_lattice_exchange(int mode);
 
 /*
  * Testing support for the bounded waits of the multi-band lattice passes
@@ -297,7 +309,8 @@ int tdt_loss_set_lattice_bands(int bands);
  * later calls in GPU clock cycles (0: the default, about one second).
  * utterance < 0 switches the fault off.  Process-wide; returns the previous
  * utterance setting (-1: none).  Only multi-band lattices wait at all
- * (tdt_loss_set_lattice_bands(K >= 2), or lattices too tall for one CTA).
+ * (tdt_loss_set_lattice_bands(K >= 2), or lattices too tall for one CTA),
+ * with either exchange.
  */
 long long tdt_loss_test_set_halo_fault(long long utterance, long long wait_limit_cycles);
 

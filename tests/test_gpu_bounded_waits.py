@@ -36,8 +36,11 @@ def _run(binding, inp, compute_grad=True):
     return loss.double().cpu().numpy(), grad
 
 
+@pytest.mark.parametrize("exchange", [1, 2])
 @pytest.mark.parametrize("faulted", [0, 2])
-def test_wait_runs_out_and_marks_only_that_utterance(binding, oracle_mod, faulted):
+def test_wait_runs_out_and_marks_only_that_utterance(binding, oracle_mod, faulted, exchange):
+    """exchange 1: bands in a thread-block cluster (mbarrier waits);
+    exchange 2: bands exchanging through global memory (polled entries)."""
     w = scaled(WORKLOADS["tiny"], name="halo_fault", B=3, T=40, U=100, V=50, blank=49,
                durations=(0, 1, 2, 3), dtype="f32", std=1.0, sigma=0.05, reduction="none",
                seed=2718)
@@ -46,6 +49,7 @@ def test_wait_runs_out_and_marks_only_that_utterance(binding, oracle_mod, faulte
                               inp["logit_lens"].cpu().numpy(), inp["label_lens"].cpu().numpy(),
                               inp["durations"], inp["blank"], inp["sigma"], "none")
     prev_bands = binding.tdt_loss_set_lattice_bands(4)
+    prev_mode = binding.tdt_loss_set_lattice_exchange(exchange)
     try:
         assert binding.tdt_loss_test_set_halo_fault(faulted, LIMIT_CYCLES) == -1
         try:
@@ -68,3 +72,4 @@ def test_wait_runs_out_and_marks_only_that_utterance(binding, oracle_mod, faulte
         assert np.abs(grad2.double().cpu().numpy() - ref.grad).max() <= 1e-5
     finally:
         binding.tdt_loss_set_lattice_bands(prev_bands)
+        binding.tdt_loss_set_lattice_exchange(prev_mode)

@@ -362,22 +362,27 @@ BANDED = {
 
 @pytest.mark.parametrize("name", sorted(BANDED))
 def test_lattice_bands_do_not_change_results(binding, oracle_mod, record_margin, name):
-    """The lattice rows are split into K bands (one CTA each, a thread-block
-    cluster); the arithmetic per node is the same for every K, so the loss and
-    the gradient must agree bit for bit, and with the oracle."""
+    """The lattice rows are split into K bands (one CTA each) that exchange
+    boundary rows in a thread-block cluster (exchange 1) or through global
+    memory (exchange 2); the arithmetic per node is the same for every K and
+    either exchange, so the loss and the gradient must agree bit for bit, and
+    with the oracle."""
     w = scaled(WORKLOADS["tiny"], name="bands_" + name, seed=4242, **BANDED[name])
     inp = make_inputs(w, device="cuda")
     results = []
-    for K in (0, 1, 2, 3, 7, 16):
+    cases = [(K, 0) for K in (0, 1, 2, 3, 7, 16)] + [(K, 2) for K in (2, 3, 7, 24, 80)]
+    for K, mode in cases:
         prev = binding.tdt_loss_set_lattice_bands(K)
+        prev_mode = binding.tdt_loss_set_lattice_exchange(mode)
         try:
             loss, grad = run_gpu(binding, inp)
         finally:
             binding.tdt_loss_set_lattice_bands(prev)
-        results.append((K, loss.clone(), grad.clone()))
-    for K, loss, grad in results[1:]:
-        assert torch.equal(loss, results[0][1]), "loss differs with %d bands" % K
-        assert torch.equal(grad, results[0][2]), "grad differs with %d bands" % K
+            binding.tdt_loss_set_lattice_exchange(prev_mode)
+        results.append(((K, mode), loss.clone(), grad.clone()))
+    for case, loss, grad in results[1:]:
+        assert torch.equal(loss, results[0][1]), "loss differs with bands/exchange %s" % (case,)
+        assert torch.equal(grad, results[0][2]), "grad differs with bands/exchange %s" % (case,)
     ref = run_oracle(oracle_mod, inp)
 
     def margin(q, e, t):

@@ -39,14 +39,14 @@ def workspace_nbytes(B, T, U1, n_dur):
     torch.compile: per anti-diagonal slot a node arc record of 2 * D arc
     probabilities, alpha and beta (8 bytes each: int32 exponent, float32
     mantissa) and a record of 2 + D arc fractions (float32); per node two
-    log-sum-exps; per utterance likelihood, scale and flag; every region
-    256-byte aligned.
+    log-sum-exps; per utterance likelihood, scale, flag and the lattice
+    launch's start counter; every region 256-byte aligned.
     """
     ndiag = B * (T + U1 - 1) * U1
     nodes = B * T * U1
     rec_len = 2 * n_dur
     regions = (ndiag * 8 * rec_len, ndiag * 8, ndiag * 8, nodes * 4, nodes * 4,
-               ndiag * 4 * (2 + n_dur), B * 8, B * 4, B * 4)
+               ndiag * 4 * (2 + n_dur), B * 8, B * 4, B * 4, B * 4)
     off = 0
     for r in regions:
         off = _align(off + r)

@@ -60,6 +60,8 @@ def _load() -> ctypes.CDLL:
     lib.tdt_loss_version.argtypes = []
     lib.tdt_loss_set_lattice_bands.restype = I
     lib.tdt_loss_set_lattice_bands.argtypes = [I]
+    lib.tdt_loss_set_lattice_exchange.restype = I
+    lib.tdt_loss_set_lattice_exchange.argtypes = [I]
     lib.tdt_loss_test_set_halo_fault.restype = ctypes.c_longlong
     lib.tdt_loss_test_set_halo_fault.argtypes = [ctypes.c_longlong, ctypes.c_longlong]
     lib.tdt_loss_timing_enable.restype = None
@@ -278,6 +280,13 @@ def tdt_loss_set_lattice_bands(bands: int) -> int:
     """Force K bands (CTAs per utterance and direction) in the lattice passes;
     0 = automatic.  Results do not depend on K.  Returns the previous value."""
     return int(lib.tdt_loss_set_lattice_bands(int(bands)))
+
+
+def tdt_loss_set_lattice_exchange(mode: int) -> int:
+    """How lattice bands exchange boundary rows: 0 = automatic, 1 = a
+    thread-block cluster, 2 = global memory.  Results do not depend on it.
+    Returns the previous value."""
+    return int(lib.tdt_loss_set_lattice_exchange(int(mode)))
 
 
 def tdt_loss_test_set_halo_fault(utterance: int, wait_limit_cycles: int = 0) -> int:

@@ -62,6 +62,7 @@ bool make_layout(const int64_t sizes[4], int n_dur, Layout *L) {
   L->loglik = take((size_t)B * sizeof(LV));
   L->scale = take((size_t)B * 4);
   L->usable = take((size_t)B * 4);
+  L->ticket = take((size_t)B * 4);
   L->total = off > 0 ? off : 256;
   return true;
 }
@@ -78,6 +79,7 @@ Workspace carve(const Layout &L, void *base) {
   w.loglik = reinterpret_cast<LV *>(c + L.loglik);
   w.scale = reinterpret_cast<float *>(c + L.scale);
   w.usable = reinterpret_cast<int *>(c + L.usable);
+  w.ticket = reinterpret_cast<int *>(c + L.ticket);
   return w;
 }
 
@@ -157,6 +159,7 @@ int validate(const void *logits, const int64_t sizes[4], const int64_t strides[4
   p->rnnt = rnnt ? 1 : 0;
   fast_div_setup(T, &p->divT_m, &p->divT_s);
   fast_div_setup(U1, &p->divU1_m, &p->divU1_s);
+  p->gx_rows = 0;
   return TDT_OK;
 }
 
@@ -301,10 +304,12 @@ int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void 
   const long long logit_bytes = p.B * rows_per_utt * p.VD * (dtype == kF32 ? 4 : 2);
   if (logit_bytes < kSerialBytes) {
     const long long rows = p.B * rows_per_utt;
+    Problem ps = p;
+    ps.gx_rows = lattice_global_rows(p, p.B);
     TDT_TRY(timed(TDT_KERNEL_TABLES, stream,
-                  [&] { return launch_node_tables(p, dtype, ws, 0, rows, stream); }));
+                  [&] { return launch_node_tables(ps, dtype, ws, 0, rows, stream); }));
     TDT_TRY(timed(TDT_KERNEL_LATTICE, stream,
-                  [&] { return launch_lattice(p, ws, 0, p.B, coeffs, stream); }));
+                  [&] { return launch_lattice(ps, ws, 0, p.B, coeffs, stream); }));
     TDT_TRY(timed(TDT_KERNEL_REDUCE, stream, [&] { return launch_reduce(p, ws, loss_out, stream); }));
     if (with_grad)
       TDT_TRY(timed(TDT_KERNEL_GRAD, stream, [&] {
@@ -330,14 +335,18 @@ int run(const Problem &p, int dtype, const Workspace &ws, float *loss_out, void 
     if (c == 1 || (c > 1 && b1 - b0 < 2))
       TDT_TRY(cudaStreamWaitEvent(ts, res->tables_done[c - 1], 0));
     if (c == 1 && started_used) TDT_TRY(cudaStreamWaitEvent(ts, res->started[0], 0));
+    // the band plan of this chunk's lattice: its node tables clear the
+    // boundary rows that the bands exchange through global memory
+    Problem pc = p;
+    pc.gx_rows = lattice_global_rows(p, b1 - b0);
     TDT_TRY(timed(TDT_KERNEL_TABLES, ts, [&] {
-      return launch_node_tables(p, dtype, ws, b0 * rows_per_utt, b1 * rows_per_utt, ts);
+      return launch_node_tables(pc, dtype, ws, b0 * rows_per_utt, b1 * rows_per_utt, ts);
     }));
     TDT_TRY(cudaEventRecord(res->tables_done[c], ts));
     TDT_TRY(cudaStreamWaitEvent(side, res->tables_done[c], 0));
     started_used = false;
     TDT_TRY(timed(TDT_KERNEL_LATTICE, side, [&] {
-      return launch_lattice(p, ws, b0, b1, coeffs, side,
+      return launch_lattice(pc, ws, b0, b1, coeffs, side,
                             c == 0 && nchunk > 1 ? res->started[0] : nullptr, &started_used);
     }));
     TDT_TRY(cudaEventRecord(res->lattice_done[c], side));

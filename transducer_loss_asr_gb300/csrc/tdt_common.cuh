@@ -68,6 +68,10 @@ struct Problem {
                                   //    its boundary row (-1: none; set by launch_lattice)
   unsigned divT_m, divU1_m;       // n / T and n / U1 for n < 2^31 as (n m) >> s
   int divT_s, divU1_s;            //    (set by the host, fast_div_setup)
+  int gx_rows;                    // > 0: the lattice bands of this launch hold gx_rows
+                                  //    rows each and exchange their boundary rows
+                                  //    through global memory (set by the host with
+                                  //    lattice_global_rows before the node tables)
 };
 
 // Division of n < 2^31 by an invariant d >= 1 with one 32 x 32 -> 64-bit
@@ -107,6 +111,16 @@ struct __align__(8) LV {
 // Exponent of a zero value: far below every non-zero value (|e| < 2^27), and
 // two of them added to a third stay in int32.
 constexpr int kXeZero = -(1 << 28);
+// No value the lattice passes store has all 64 bits zero (zero itself is
+// e = kXeZero, every other mantissa is >= 1), so all-zero bits mark a
+// boundary-row entry that its band has not written yet: the node-table pass
+// clears those entries, and the neighbouring band polls them.
+__host__ __device__ inline LV lv_unwritten() {
+  LV v;
+  v.e = 0;
+  v.s = 0.0f;
+  return v;
+}
 
 // Scratch layout (device pointers carved from one workspace block).
 struct Workspace {
@@ -126,6 +140,9 @@ struct Workspace {
   int *usable;     // [B] 1 = usable: set to 1 by the node-table pass of the
                    //   utterance's chunk, cleared by the lattice passes when the
                    //   lengths or labels are unusable or a bounded wait gave up
+  int *ticket;     // [B] start-order counter of the lattice launch whose first
+                   //   utterance is b (global-exchange bands), zeroed by the
+                   //   node-table pass
 };
 
 __host__ __device__ inline long long diag_index(const Problem &p, long long b, long long t,
@@ -247,7 +264,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 // ---- host side shared by the entry points (tdt_api.cu) ----------------------
 struct Layout {  // byte offsets of the scratch regions inside one block
-  size_t arcw, alpha, beta, lse_tok, lse_dur, frac, loglik, scale, usable, total;
+  size_t arcw, alpha, beta, lse_tok, lse_dur, frac, loglik, scale, usable, ticket, total;
 };
 bool make_layout(const int64_t sizes[4], int n_dur, Layout *L);
 Workspace carve(const Layout &L, void *base);
@@ -265,6 +282,12 @@ cudaError_t launch_node_tables(const Problem &p, int dtype, const Workspace &ws,
 // launch has begun (a launch-completion event); *started_used tells whether
 // it was attached (the plain fallback kernels and launches of more than
 // 65535 utterances do not record it).
+// Rows per band when the lattice of a launch of nb utterances splits into
+// bands exchanging through global memory, else 0.  The caller stores it in
+// Problem::gx_rows before the node-table pass of those utterances (which
+// clears the boundary rows and the start counter) and passes the same
+// Problem to launch_lattice.
+int lattice_global_rows(const Problem &p, long long nb);
 cudaError_t launch_lattice(const Problem &p, const Workspace &ws, long long b_begin,
                            long long b_end, bool with_beta, cudaStream_t stream,
                            cudaEvent_t started = nullptr, bool *started_used = nullptr);

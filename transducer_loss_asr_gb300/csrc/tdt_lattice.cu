@@ -32,6 +32,15 @@
 //    so neighbouring bands run a few diagonals apart with no cluster-wide
 //    barrier per diagonal.  Every wait is bounded: past the limit the
 //    utterance is marked unusable (NaN loss) and the CTA stops.
+//    Lattices too tall for one CTA instead split into many small bands (two
+//    warps each, ~30 rows) that are not a cluster: a band's boundary row
+//    goes to its neighbour through global memory.  The node-table pass
+//    clears those boundary entries to all-zero bits, which no lattice value
+//    has; the producing lane stores each value with a gpu-scope relaxed
+//    64-bit store, and one thread of the consuming band loads it one step
+//    before it is needed (polling, bounded, when it is not written yet).
+//    CTAs take their band from a start-order ticket, so a band only waits
+//    on bands that started before it.
 //  * alpha_kernel / beta_kernel: the same wavefront reading and writing
 //    global memory, any U and D (no limit on label length).
 #include <atomic>
@@ -48,6 +57,9 @@ extern __shared__ __align__(16) unsigned char tdt_dyn_smem[];
 
 // Band count forced by tdt_loss_set_lattice_bands (0: chosen per problem).
 std::atomic<int> g_forced_bands{0};
+// How bands exchange boundary rows, forced by tdt_loss_set_lattice_exchange
+// (0: chosen per problem, 1: thread-block cluster, 2: global memory).
+std::atomic<int> g_forced_exchange{0};
 // Testing support (tdt_loss_test_set_halo_fault): the utterance whose band 1
 // withholds its boundary row (-1: none) and the wait limit in clock cycles
 // (0: kWaitLimitCycles).
@@ -309,14 +321,62 @@ __device__ __forceinline__ void arrive_cluster_relaxed(unsigned bar_addr) {
 // long_labels (D = 9) 0.915 / 0.853 / 0.893 / 1.058 us.
 constexpr int group_lanes(int nd) { return nd <= 5 ? 1 : 2; }
 
+// How the bands of an utterance exchange boundary rows.
+enum Exchange {
+  kXNone = 0,     // one band: no exchange
+  kXCluster = 1,  // a thread-block cluster: distributed shared memory + mbarriers
+  kXGlobal = 2,   // any number of bands: global memory, polled
+};
+
+// ---- global-memory exchange (PTX ISA memory consistency model: relaxed
+// strong operations at gpu scope; an aligned 64-bit access is single-copy
+// atomic, so a reader sees either the cleared word or the whole value)
+__device__ __forceinline__ void st_relaxed_gpu_lv(LV *p, const LV &v) {
+  const unsigned long long w =
+      (unsigned long long)(unsigned)v.e | ((unsigned long long)__float_as_uint(v.s) << 32);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_bits(const LV *p) {
+  unsigned long long w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+__device__ __forceinline__ LV lv_from_bits(unsigned long long w) {
+  LV v;
+  v.e = (int)(unsigned)w;
+  v.s = __uint_as_float((unsigned)(w >> 32));
+  return v;
+}
+// Poll the boundary-row entry at p until it is written (not all-zero bits),
+// for at most `limit` clock cycles; false on timeout.
+__device__ __forceinline__ bool poll_written_bounded(const LV *p, long long limit,
+                                                     unsigned long long *w) {
+  unsigned long long x = ld_relaxed_gpu_bits(p);
+  if (x != 0ull) {
+    *w = x;
+    return true;
+  }
+  const long long t0 = clock64();
+  do {
+    x = ld_relaxed_gpu_bits(p);
+    if (x != 0ull) {
+      *w = x;
+      return true;
+    }
+  } while (clock64() - t0 <= limit);
+  return false;
+}
+
 // Launch-time shape of the cluster variant.
 struct ClusterPlan {
-  int K;        // CTAs per (utterance, direction): the cluster size
+  int X;        // Exchange: kXNone (K = 1), kXCluster or kXGlobal
+  int dirs;     // directions per utterance in the launch (2: alpha and beta)
+  int K;        // CTAs per (utterance, direction): the bands (cluster size for kXCluster)
   int Rc;       // lattice rows per CTA
   int G;        // lanes per node
   int RA, RW;   // slots of the value ring and of the record ring (powers of two)
   int P;        // prefetch distance in diagonals (kPrefetchDeep or kPrefetch)
-  int threads;  // (Rc + 1) * G rounded up to whole warps, plus a control warp if K > 1
+  int threads;  // (Rc + 1) * G rounded up to whole warps, plus a control warp for kXCluster
   size_t smem;  // shared bytes used
 };
 
@@ -447,10 +507,11 @@ struct Band {
 // j - RA before storing.  The control warp issues no global stores and no
 // compute; it copies the arc records into the record ring.
 
-template <int ND, int G, bool MULTI, int P>
+template <int ND, int G, int X, int P>
 __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace &ws,
                                               const ClusterRings<2 * ND> r, const ClusterPlan cp,
                                               const Band bd, long long b) {
+  constexpr bool MULTI = X == kXCluster, GX = X == kXGlobal;
   constexpr int REC = 2 * ND;
   constexpr int J = (ND + G - 1) / G;
   const int row = bd.row, k = bd.lane;
@@ -458,7 +519,7 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
   const int rl = rowc >= 1 ? rowc - 1 : 0;
   const int u = bd.u_lo + row - 1;
   const bool own = row >= 1 && row <= cp.Rc;
-  const bool lower = MULTI && bd.k > 0, upper = MULTI && bd.k + 1 < bd.K;
+  const bool lower = (MULTI || GX) && bd.k > 0, upper = (MULTI || GX) && bd.k + 1 < bd.K;
   const LV *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * REC;
   LV *galpha = ws.alpha + b * p.n_diag * p.U1;
   // lane k takes durations k, k + G, ...; with G not dividing ND the last
@@ -479,7 +540,17 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
   const int plane = threadIdx.x & 31;
   // feeds the upper band (testing: band 1 of utterance fault_utt never does,
   // so the upper band's bounded wait runs out)
-  const bool producer = upper && row == cp.Rc && k == 0 && !(bd.k == 1 && b == p.fault_utt);
+  const bool feeds = !(bd.k == 1 && b == p.fault_utt);
+  const bool producer = MULTI && upper && row == cp.Rc && k == 0 && feeds;
+  // global exchange: the top row's lane 0 stores its values with gpu-scope
+  // relaxed stores (the upper band polls them), and thread 0 (ring row 0,
+  // whose lanes compute nothing they keep) brings row u_lo - 1 of the lower
+  // band into ring row 0, each value loaded one step before it is needed
+  const bool gx_top = GX && upper && row == cp.Rc && k == 0;
+  const bool gx_halo = GX && lower && threadIdx.x == 0;
+  const int uh = bd.u_lo - 1;  // the lower band's top row
+  const LV *halo_src = galpha + uh;
+  unsigned long long pend = 0ull;  // bits of (diagonal s - 1, uh), loaded in step s - 1
   int failed = 0;  // a bounded wait of this thread gave up
   auto prefetch = [&](int q) {
     if (MULTI) {
@@ -503,13 +574,33 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
       if (!wait_parity_bounded(r.full((s - 1) & r.mA), ((s - 1) / r.RA) & 1, p.wait_limit))
         failed = 1;
     }
+    if (gx_halo) {
+      if (s >= 1) {
+        // (s - 1, uh) is a node iff its frame s - 1 - uh lies in [0, T_b)
+        LV hv = xf_zero();
+        const int th = s - 1 - uh;
+        if (th >= 0 && th < bd.Tb && uh <= bd.Ub) {
+          unsigned long long w = pend;
+          if (w == 0ull &&
+              !poll_written_bounded(halo_src + (long long)(s - 1) * bd.U1, p.wait_limit, &w))
+            failed = 1;
+          hv = lv_from_bits(w);
+        }
+        r.a(s - 1, 0) = hv;
+      }
+      // the next step's value, in flight while this step computes
+      const int tn = s - uh;
+      pend = (tn >= 0 && tn < bd.Tb && uh <= bd.Ub)
+                 ? ld_relaxed_gpu_bits(halo_src + (long long)s * bd.U1)
+                 : 0ull;
+    }
     // a thread whose wait gave up raises the CTA's abort flag before the
     // barrier (every write to it precedes one), and all leave together after
     // it; a plain barrier and a flag read cost less per diagonal than a
     // barrier with a reduction (measured: long_labels lattice 4.79 vs 4.85 ms)
-    if (MULTI && failed) *bd.abort = 1;
+    if ((MULTI || GX) && failed) *bd.abort = 1;
     __syncthreads();
-    if (MULTI && *bd.abort) break;
+    if ((MULTI || GX) && *bd.abort) break;
     // the slot of diagonal s - 1 serves diagonal s - 1 + RA next
     if (MULTI && bd.control && lower && s >= 1 && s - 1 + r.RA <= nsteps - 2)
       arrive_expect_tx(r.full((s - 1) & r.mA), (unsigned)sizeof(LV));
@@ -541,7 +632,10 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     // every lane of the group holds the node's value; lane 0 stores it
     const LV v = node ? (s == 0 ? xf_one() : xf_from_sum(tot, es)) : xf_zero();
     if (own && k == 0) r.a(s, row) = v;
-    if (node && k == 0) galpha[(long long)s * bd.U1 + u] = v;
+    if (node && k == 0) {
+      if (!gx_top) galpha[(long long)s * bd.U1 + u] = v;
+      else if (feeds) st_relaxed_gpu_lv(galpha + (long long)s * bd.U1 + u, v);
+    }
     if (producer) {
       // publish this diagonal's top row into the upper band's halo slot once
       // that band has released the slot's previous diagonal
@@ -553,24 +647,25 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     }
   }
   cp_async_wait<0>();
-  if (MULTI) {
+  if (MULTI || GX) {
     if (__syncthreads_or(failed) && threadIdx.x == 0) *bd.abort = 1;
   } else {
     __syncthreads();
   }
 }
 
-template <int ND, int G, bool MULTI, int P>
+template <int ND, int G, int X, int P>
 __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &ws,
                                              const ClusterRings<2 * ND> r, const ClusterPlan cp,
                                              const Band bd, long long b) {
+  constexpr bool MULTI = X == kXCluster, GX = X == kXGlobal;
   constexpr int REC = 2 * ND;
   constexpr int J = (ND + G - 1) / G;
   const int row = bd.row, k = bd.lane;
   const int rowc = row <= cp.Rc ? row : cp.Rc;
   const int u = bd.u_lo + row - 1;
   const bool own = row >= 1 && row <= cp.Rc;
-  const bool lower = MULTI && bd.k > 0, upper = MULTI && bd.k + 1 < bd.K;
+  const bool lower = (MULTI || GX) && bd.k > 0, upper = (MULTI || GX) && bd.k + 1 < bd.K;
   const LV *gdiag0 = ws.arcw + b * p.n_diag * p.U1 * REC;
   LV *gbeta = ws.beta + b * p.n_diag * p.U1;
   float *gfrac = ws.frac + b * p.n_diag * p.U1 * (2 + ND);
@@ -589,7 +684,16 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
   const bool pref = MULTI ? bd.prefetch_warp : own;
   const int plane = threadIdx.x & 31;
   // feeds the lower band (testing: band 1 of utterance fault_utt never does)
-  const bool producer = lower && row == 1 && k == 0 && !(bd.k == 1 && b == p.fault_utt);
+  const bool feeds = !(bd.k == 1 && b == p.fault_utt);
+  const bool producer = MULTI && lower && row == 1 && k == 0 && feeds;
+  // global exchange, as in the alpha pass: the bottom row's lane 0 stores
+  // with gpu-scope relaxed stores, thread 0 (ring row 0 is unused here)
+  // brings row u_lo + Rc of the upper band into ring row Rc + 1
+  const bool gx_bottom = GX && lower && row == 1 && k == 0;
+  const bool gx_halo = GX && upper && threadIdx.x == 0;
+  const int uh = bd.u_lo + cp.Rc;  // the upper band's bottom row
+  const LV *halo_src = gbeta + uh;
+  unsigned long long pend = 0ull;  // bits of (diagonal q + 1, uh), loaded in the step before
   int failed = 0;  // a bounded wait of this thread gave up
   auto prefetch = [&](int q) {
     if (MULTI) {
@@ -618,13 +722,33 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
       if (!wait_parity_bounded(r.full((i - 1) & r.mA), ((i - 1) / r.RA) & 1, p.wait_limit))
         failed = 1;
     }
+    if (gx_halo) {
+      if (i >= 1) {
+        // (q + 1, uh) is a node iff its frame q + 1 - uh lies in [0, T_b)
+        LV hv = xf_zero();
+        const int th = q + 1 - uh;
+        if (th >= 0 && th < bd.Tb && uh <= bd.Ub) {
+          unsigned long long w = pend;
+          if (w == 0ull &&
+              !poll_written_bounded(halo_src + (long long)(q + 1) * bd.U1, p.wait_limit, &w))
+            failed = 1;
+          hv = lv_from_bits(w);
+        }
+        r.a(q + 1, cp.Rc + 1) = hv;
+      }
+      // the next step's value (diagonal q), in flight while this step computes
+      const int tn = q - uh;
+      pend = (tn >= 0 && tn < bd.Tb && uh <= bd.Ub)
+                 ? ld_relaxed_gpu_bits(halo_src + (long long)q * bd.U1)
+                 : 0ull;
+    }
     // a thread whose wait gave up raises the CTA's abort flag before the
     // barrier (every write to it precedes one), and all leave together after
     // it; a plain barrier and a flag read cost less per diagonal than a
     // barrier with a reduction (measured: long_labels lattice 4.79 vs 4.85 ms)
-    if (MULTI && failed) *bd.abort = 1;
+    if ((MULTI || GX) && failed) *bd.abort = 1;
     __syncthreads();
-    if (MULTI && *bd.abort) break;
+    if ((MULTI || GX) && *bd.abort) break;
     // the slot of step i - 1 serves step i - 1 + RA next
     if (MULTI && bd.control && upper && i >= 1 && i - 1 + r.RA <= nsteps - 2)
       arrive_expect_tx(r.full((i - 1) & r.mA), (unsigned)sizeof(LV));
@@ -677,7 +801,8 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     if (node && k == 0) {
       fr[0] = fb * inv;
       fr[1] = fl * inv;
-      gbeta[(long long)q * bd.U1 + u] = v;
+      if (!gx_bottom) gbeta[(long long)q * bd.U1 + u] = v;
+      else if (feeds) st_relaxed_gpu_lv(gbeta + (long long)q * bd.U1 + u, v);
     }
     if (producer) {
       // publish this diagonal's bottom row into the lower band's halo slot
@@ -690,7 +815,7 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     }
   }
   cp_async_wait<0>();
-  if (MULTI) {
+  if (MULTI || GX) {
     if (__syncthreads_or(failed) && threadIdx.x == 0) *bd.abort = 1;
   } else {
     __syncthreads();
@@ -698,21 +823,45 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
 }
 
 // Block: (Rc + 1) * G compute threads (rounded up to whole warps), then,
-// with neighbouring bands, one control warp: it copies the arc records and
-// waits for and releases the halo slots.
-template <int ND, int G, bool MULTI, int P>
-__global__ void __launch_bounds__(MULTI ? kLatticeMaxThreads : kLatticeOneBandThreads, 1)
+// with cluster bands, one control warp: it copies the arc records and waits
+// for and releases the halo slots.
+//
+// Global-exchange bands (X = kXGlobal) are CTAs of a one-dimensional grid
+// that take their role from a start-order ticket (an atomic counter that
+// the node-table pass zeroed): ticket j of an utterance is alpha band j / 2
+// or beta band K - 1 - j / 2, so a band's only producer (alpha: the band
+// below, beta: the band above) has a smaller ticket, has started before it
+// and is resident.  A band therefore waits only on resident CTAs that never
+// wait on it: no residency assumption, whatever else runs on the GPU.
+template <int ND, int G, int X, int P>
+__global__ void __launch_bounds__(X == kXCluster ? kLatticeMaxThreads : kLatticeOneBandThreads, 1)
 lattice_cluster_kernel(Problem p, Workspace ws, long long b0, ClusterPlan cp) {
+  constexpr bool MULTI = X == kXCluster, GX = X == kXGlobal;
   constexpr int REC = 2 * ND;
   __shared__ int s_abort;
-  const long long b = b0 + blockIdx.y;
-  const bool is_beta = blockIdx.z == 1;
-  const int kc = (int)cluster_rank();
+  __shared__ int s_ticket;
+  long long b;
+  bool is_beta;
+  int kc;
+  if (GX) {
+    if (threadIdx.x == 0) s_ticket = atomicAdd(ws.ticket + b0, 1);
+    __syncthreads();
+    const int per = cp.dirs * cp.K, rem = s_ticket % per, j = cp.dirs == 2 ? rem >> 1 : rem;
+    b = b0 + s_ticket / per;
+    is_beta = cp.dirs == 2 && (rem & 1);
+    kc = is_beta ? cp.K - 1 - j : j;
+  } else {
+    b = b0 + blockIdx.y;
+    is_beta = blockIdx.z == 1;
+    kc = MULTI ? (int)cluster_rank() : 0;
+  }
   double sum_u;
   // every CTA of the cluster sees the same utterance, so all return together
   const bool ok = check_utterance(p, b, &sum_u);
   if (!is_beta && kc == 0 && threadIdx.x == 0) write_utterance_info(p, ws, b, ok, sum_u);
   if (!ok) return;
+  // a global-exchange band wholly above U_b has no node and feeds no node
+  if (GX && (long long)kc * cp.Rc > p.label_lens[b]) return;
   ClusterRings<REC> r;
   r.RA = cp.RA;
   r.mA = cp.RA - 1;
@@ -721,7 +870,7 @@ lattice_cluster_kernel(Problem p, Workspace ws, long long b0, ClusterPlan cp) {
   r.slotW = (cp.Rc + 1) * REC * 8;
   r.offW = (unsigned)(cp.RA * r.slotA);
   r.offBar = r.offW + (unsigned)(cp.RW * r.slotW);
-  const int compute_threads = cp.threads - (cp.K > 1 ? 32 : 0);
+  const int compute_threads = cp.threads - (MULTI ? 32 : 0);
   // both rings start as zeros (exponent kXeZero, mantissa 0), so arcs from
   // or to slots not yet written contribute nothing; every region is a whole
   // number of 16-byte chunks
@@ -758,10 +907,10 @@ lattice_cluster_kernel(Problem p, Workspace ws, long long b0, ClusterPlan cp) {
   bd.Ub = (int)p.label_lens[b];
   bd.U1 = (int)p.U1;
   bd.abort = &s_abort;
-  if (!is_beta) alpha_cluster<ND, G, MULTI, P>(p, ws, r, cp, bd, b);
-  else beta_cluster<ND, G, MULTI, P>(p, ws, r, cp, bd, b);
+  if (!is_beta) alpha_cluster<ND, G, X, P>(p, ws, r, cp, bd, b);
+  else beta_cluster<ND, G, X, P>(p, ws, r, cp, bd, b);
   __syncthreads();
-  if (MULTI && s_abort && threadIdx.x == 0) ws.usable[b] = 0;  // a wait timed out: NaN loss
+  if ((MULTI || GX) && s_abort && threadIdx.x == 0) ws.usable[b] = 0;  // a wait timed out: NaN loss
   // no band leaves while a neighbour may still write into its shared memory
   if (MULTI) cluster_sync_all();
   if (!is_beta && threadIdx.x == 0 && !s_abort && bd.Ub >= bd.u_lo &&
@@ -785,22 +934,30 @@ int pow2_at_least(int v) {
 constexpr int kMaxCluster = 16;
 constexpr size_t kClusterSmemMax = 220 * 1024;
 
-// Shape of the cluster variant for this problem with K bands, or false.
-bool cluster_plan(const Problem &p, int K, ClusterPlan *cp) {
+// Shape of the banded variant for this problem with K bands exchanging by
+// X (K = 1: kXNone), or false.
+bool cluster_plan(const Problem &p, int K, int X, ClusterPlan *cp) {
   if (p.n_dur > 9) return false;
+  if (K == 1) X = kXNone;
+  if (K > 1 && X == kXNone) return false;
   const int G = group_lanes(p.n_dur);
   const int Rc = (int)((p.U1 + K - 1) / K);
-  const int threads = ((Rc + 1) * G + 31) / 32 * 32 + (K > 1 ? 32 : 0);
-  if (threads > (K > 1 ? kLatticeMaxThreads : kLatticeOneBandThreads)) return false;
+  K = (int)((p.U1 + Rc - 1) / Rc);  // no band without rows
+  const int threads = ((Rc + 1) * G + 31) / 32 * 32 + (X == kXCluster ? 32 : 0);
+  if (threads > (X == kXCluster ? kLatticeMaxThreads : kLatticeOneBandThreads)) return false;
+  if (X == kXCluster && K == 1) return false;
   const int rec = arc_record_len(p.n_dur);
   // value ring: max_dur + 2 diagonals in use, the rest is how far a band may
   // run ahead of the band it feeds
   const int RA = pow2_at_least(p.max_dur + 10);
-  // the deeper prefetch for a single band when its record ring still fits
-  for (int P : {K == 1 ? kPrefetchDeep : kPrefetch, kPrefetch}) {
+  // the deeper prefetch for bands without a control warp when its record
+  // ring still fits
+  for (int P : {X != kXCluster ? kPrefetchDeep : kPrefetch, kPrefetch}) {
     const int RW = pow2_at_least(P + p.max_dur + 3);
     const size_t bytes = cluster_smem_bytes(RA, RW, Rc, rec);
     if (bytes > kClusterSmemMax) continue;
+    cp->X = X;
+    cp->dirs = 2;
     cp->K = K;
     cp->Rc = Rc;
     cp->G = G;
@@ -833,22 +990,69 @@ int preferred_bands(const Problem &p, long long nb) {
   return K < kMaxCluster ? K : kMaxCluster;
 }
 
+// Lanes of a global-exchange band and the CTAs of such a launch.  A band of
+// two warps steps a diagonal about as fast as the one-band lattices of ~40
+// rows, and its neighbour's value reaches it through L2 one step later;
+// the launch takes at most kGlobalBandCtas SMs.
+constexpr int kGlobalBandLanes = 64;
+constexpr int kGlobalBandCtas = 128;
+
+}  // namespace
+
+int lattice_global_rows(const Problem &p, long long nb) {
+  if (p.n_dur > 9 || nb < 1) return 0;
+  const int mode = g_forced_exchange.load();
+  if (mode == kXCluster) return 0;
+  const int G = group_lanes(p.n_dur);
+  const int forced = g_forced_bands.load();
+  int K;
+  if (forced > 0) {
+    // forced counts up to a cluster's size use a cluster unless global
+    // exchange is forced too
+    if (forced == 1 || (forced <= kMaxCluster && mode != kXGlobal)) return 0;
+    K = forced;
+  } else {
+    const int warps = (int)(((p.U1 + 1) * G + 31) / 32);
+    if (warps <= 16) return 0;  // one band
+    const int rows = kGlobalBandLanes / G - 1;
+    K = (int)((p.U1 + rows - 1) / rows);
+    const long long cap = kGlobalBandCtas / (2 * nb);
+    if (K > cap) K = cap > 1 ? (int)cap : 1;
+    if (K < 2) return 0;
+  }
+  ClusterPlan cp;
+  if (!cluster_plan(p, K, kXGlobal, &cp)) return 0;
+  return cp.Rc;
+}
+
+namespace {
+
 template <int ND, int G>
 cudaError_t launch_cluster_g(const Problem &p, const Workspace &ws, long long b0, long long nb,
-                             bool with_beta, const ClusterPlan &cp, cudaStream_t stream,
+                             bool with_beta, const ClusterPlan &cp_in, cudaStream_t stream,
                              bool *placed, cudaEvent_t started, bool *started_used) {
   *placed = false;
-  auto kern = cp.K > 1 ? lattice_cluster_kernel<ND, G, true, kPrefetch>
-                       : (cp.P == kPrefetchDeep ? lattice_cluster_kernel<ND, G, false, kPrefetchDeep>
-                                                : lattice_cluster_kernel<ND, G, false, kPrefetch>);
+  ClusterPlan cp = cp_in;
+  cp.dirs = with_beta ? 2 : 1;
+  auto kern =
+      cp.X == kXCluster
+          ? lattice_cluster_kernel<ND, G, kXCluster, kPrefetch>
+          : cp.X == kXGlobal
+                ? (cp.P == kPrefetchDeep ? lattice_cluster_kernel<ND, G, kXGlobal, kPrefetchDeep>
+                                         : lattice_cluster_kernel<ND, G, kXGlobal, kPrefetch>)
+                : (cp.P == kPrefetchDeep ? lattice_cluster_kernel<ND, G, kXNone, kPrefetchDeep>
+                                         : lattice_cluster_kernel<ND, G, kXNone, kPrefetch>);
   // at least kLatticeSmemFloor, so no node-table or gradient block shares the SM
   const size_t bytes = cp.smem < (size_t)kLatticeSmemFloor ? (size_t)kLatticeSmemFloor : cp.smem;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess && cp.K > 8)
+  if (e == cudaSuccess && cp.X == kXCluster && cp.K > 8)
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
-  const dim3 grid((unsigned)cp.K, (unsigned)nb, with_beta ? 2u : 1u);
+  // global-exchange bands: one-dimensional, roles by start-order ticket
+  const dim3 grid = cp.X == kXGlobal
+                        ? dim3((unsigned)(cp.K * cp.dirs * nb), 1u, 1u)
+                        : dim3((unsigned)cp.K, (unsigned)nb, (unsigned)cp.dirs);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3((unsigned)cp.threads, 1, 1);
@@ -862,8 +1066,9 @@ cudaError_t launch_cluster_g(const Problem &p, const Workspace &ws, long long b0
     attr[na].val.launchCompletionEvent.flags = 0;
     ++na;
   }
-  if (cp.K == 1) {
-    // one band: an ordinary launch (a CTA outside a cluster is a cluster of one)
+  if (cp.X != kXCluster) {
+    // one band, or global-exchange bands: an ordinary launch (a CTA outside a
+    // cluster is a cluster of one)
     *placed = true;
     cfg.attrs = attr;
     cfg.numAttrs = na;
@@ -1005,12 +1210,25 @@ cudaError_t launch_lattice(const Problem &p_in, const Workspace &ws, long long b
     // K bands per utterance: the preferred count, else more bands (fewer
     // rows, when a band needs too many threads or too much shared memory),
     // else fewer (when a cluster of K CTAs does not fit the GPU)
+    if (p.gx_rows > 0) {
+      // bands exchanging through global memory, as planned for the node
+      // tables that cleared their boundary rows
+      ClusterPlan cp;
+      if (cluster_plan(p, (int)((p.U1 + p.gx_rows - 1) / p.gx_rows), kXGlobal, &cp) &&
+          cp.Rc == p.gx_rows) {
+        bool placed = false;
+        const cudaError_t e = launch_cluster_nd(p, ws, g0, nb, with_beta, cp, stream, &placed,
+                                                started, started_used);
+        if (e != cudaSuccess) return e;
+        done = placed;
+      }
+    }
     const int K0 = preferred_bands(p, nb);
     for (int step = 0; step < 2 * kMaxCluster && !done; ++step) {
       const int K = step < kMaxCluster - K0 + 1 ? K0 + step : K0 - (step - (kMaxCluster - K0));
       if (K < 1 || K > kMaxCluster) continue;
       ClusterPlan cp;
-      if (!cluster_plan(p, K, &cp)) continue;
+      if (!cluster_plan(p, K, kXCluster, &cp)) continue;
       bool placed = false;
       const cudaError_t e =
           launch_cluster_nd(p, ws, g0, nb, with_beta, cp, stream, &placed, started, started_used);
@@ -1038,6 +1256,11 @@ cudaError_t launch_reduce(const Problem &p, const Workspace &ws, float *loss_out
 extern "C" int tdt_loss_set_lattice_bands(int bands) {
   if (bands < 0) bands = 0;
   return tdt::g_forced_bands.exchange(bands);
+}
+
+extern "C" int tdt_loss_set_lattice_exchange(int mode) {
+  if (mode < 0 || mode > 2) mode = 0;
+  return tdt::g_forced_exchange.exchange(mode);
 }
 
 extern "C" long long tdt_loss_test_set_halo_fault(long long utterance,

@@ -120,6 +120,7 @@ extern "C" int tdt_loss_fwd_bwd_noalloc(const void *logits, const int64_t sizes[
   int rc = tdt::validate(logits, sizes, strides, dtype, labels, logit_lens, label_lens,
                          durations, n_dur, blank, sigma, reduction, loss_out, grad_out, &p, true);
   if (rc != TDT_OK) return rc;
+  p.gx_rows = tdt::lattice_global_rows(p, p.B);
   tdt::Layout L;
   if (!tdt::make_layout(sizes, n_dur, &L)) return TDT_ERR_BAD_SIZES;
   if (L.total > tdt::kNoAllocScratchBytes) return TDT_ERR_NOALLOC_TOO_LARGE;

@@ -21,7 +21,9 @@
 //                            blank and label arc probabilities per duration,
 //                            anti-diagonal layout, one contiguous record per
 //                            node for the lattice passes
-// and usable[b] = 1 for every utterance of the launch.
+// and usable[b] = 1, ticket[b] = 0 for every utterance of the launch; with
+// Problem::gx_rows > 0 also the alpha / beta entries of the band boundary
+// rows set to lv_unwritten().
 #include <type_traits>
 
 #include "tdt_rowio.cuh"
@@ -160,6 +162,16 @@ __device__ __forceinline__ void write_node_outputs(const Problem &p, const Works
   }
   if (lt == 0) ws.lse_tok[n] = rs.lse;
   if (lt == 1) ws.lse_dur[n] = p.D > 0 ? rs.lsed : 0.0f;
+  if (p.gx_rows > 0 && lt == 0) {
+    // the rows that the lattice bands of this launch hand to a neighbour
+    // through global memory (the top row of every band but the last for
+    // alpha, the bottom row of every band but the first for beta) start
+    // unwritten: the neighbour polls them until they are not
+    const long long g = diag_index(p, b, t, u);
+    const int m = (int)u % p.gx_rows;
+    if (m == p.gx_rows - 1 && u + 1 < p.U1) ws.alpha[g] = lv_unwritten();
+    if (m == 0 && u > 0) ws.beta[g] = lv_unwritten();
+  }
 }
 
 // Largest element of a batch of 16-byte vectors (those with index < nvec):
@@ -221,8 +233,10 @@ node_tables_kernel(Problem p, Workspace ws, long long n_begin, long long n_end) 
   // labels, or whose bounded wait gave up).
   if (blockIdx.x == 0) {
     const long long per_utt = p.T * p.U1;
-    for (long long bb = n_begin / per_utt + threadIdx.x; bb < n_end / per_utt; bb += blockDim.x)
+    for (long long bb = n_begin / per_utt + threadIdx.x; bb < n_end / per_utt; bb += blockDim.x) {
       ws.usable[bb] = 1;
+      ws.ticket[bb] = 0;
+    }
   }
   // The row slots of a launch walk each utterance u-major (t fastest), so
   // the RPB rows of a block share u and, with ragged label lengths, a block
