@@ -14,6 +14,16 @@ __device__ __forceinline__ unsigned smem_u32(const void *p) {
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
 }
+// 8-byte copy global -> shared if `pred` (cp.async.ca: may allocate in L1,
+// which is invalidated at every kernel launch; each address is copied once).
+// Predicated rather than branched around, so that a warp in which one lane
+// copies does not diverge.
+__device__ __forceinline__ void cp_async8_if(bool pred, void *smem, const void *gmem) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
+      "@p cp.async.ca.shared.global [%0], [%1], 8;\n\t}" ::"r"(smem_u32(smem)),
+      "l"(gmem), "r"((int)pred));
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N> __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));

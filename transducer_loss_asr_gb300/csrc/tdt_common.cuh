@@ -111,15 +111,21 @@ struct __align__(8) LV {
 // Exponent of a zero value: far below every non-zero value (|e| < 2^27), and
 // two of them added to a third stay in int32.
 constexpr int kXeZero = -(1 << 28);
-// No value the lattice passes store has all 64 bits zero (zero itself is
-// e = kXeZero, every other mantissa is >= 1), so all-zero bits mark a
-// boundary-row entry that its band has not written yet: the node-table pass
-// clears those entries, and the neighbouring band polls them.
+// A boundary-row entry that its band has not written yet (the node-table
+// pass sets the entries that lattice bands exchange to it).  Its exponent
+// is one no value has (|e| < 2^27, zero is e = kXeZero), and its mantissa
+// is 0, which a stored value has only together with e = kXeZero.  So a
+// reader that sees either half of the marker -- even next to the other half
+// of a new value -- knows the entry is not complete (lv_written).
+constexpr int kXeUnwritten = (int)0x80000000;
 __host__ __device__ inline LV lv_unwritten() {
   LV v;
-  v.e = 0;
+  v.e = kXeUnwritten;
   v.s = 0.0f;
   return v;
+}
+__host__ __device__ inline bool lv_written(const LV &v) {
+  return v.e != kXeUnwritten && (v.s != 0.0f || v.e == kXeZero);
 }
 
 // Scratch layout (device pointers carved from one workspace block).

@@ -336,6 +336,16 @@ __device__ __forceinline__ void st_relaxed_gpu_lv(LV *p, const LV &v) {
       (unsigned long long)(unsigned)v.e | ((unsigned long long)__float_as_uint(v.s) << 32);
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
+// The same if `pred` (predicated, no branch).
+__device__ __forceinline__ void st_relaxed_gpu_lv_if(bool pred, LV *p, const LV &v) {
+  const unsigned long long w =
+      (unsigned long long)(unsigned)v.e | ((unsigned long long)__float_as_uint(v.s) << 32);
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
+      "@p st.relaxed.gpu.global.b64 [%0], %1;\n\t}" ::"l"(p),
+      "l"(w), "r"((int)pred)
+      : "memory");
+}
 __device__ __forceinline__ unsigned long long ld_relaxed_gpu_bits(const LV *p) {
   unsigned long long w;
   asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
@@ -347,20 +357,19 @@ __device__ __forceinline__ LV lv_from_bits(unsigned long long w) {
   v.s = __uint_as_float((unsigned)(w >> 32));
   return v;
 }
-// Poll the boundary-row entry at p until it is written (not all-zero bits),
-// for at most `limit` clock cycles; false on timeout.
-__device__ __forceinline__ bool poll_written_bounded(const LV *p, long long limit,
-                                                     unsigned long long *w) {
-  unsigned long long x = ld_relaxed_gpu_bits(p);
-  if (x != 0ull) {
-    *w = x;
+// Poll the boundary-row entry at p until it is written (lv_written), for at
+// most `limit` clock cycles; false on timeout.
+__device__ __forceinline__ bool poll_written_bounded(const LV *p, long long limit, LV *out) {
+  LV x = lv_from_bits(ld_relaxed_gpu_bits(p));
+  if (lv_written(x)) {
+    *out = x;
     return true;
   }
   const long long t0 = clock64();
   do {
-    x = ld_relaxed_gpu_bits(p);
-    if (x != 0ull) {
-      *w = x;
+    x = lv_from_bits(ld_relaxed_gpu_bits(p));
+    if (lv_written(x)) {
+      *out = x;
       return true;
     }
   } while (clock64() - t0 <= limit);
@@ -543,19 +552,25 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
   const bool feeds = !(bd.k == 1 && b == p.fault_utt);
   const bool producer = MULTI && upper && row == cp.Rc && k == 0 && feeds;
   // global exchange: the top row's lane 0 stores its values with gpu-scope
-  // relaxed stores (the upper band polls them), and thread 0 (ring row 0,
-  // whose lanes compute nothing they keep) brings row u_lo - 1 of the lower
-  // band into ring row 0, each value loaded one step before it is needed
+  // relaxed stores, and thread 0 (ring row 0, whose lanes compute nothing
+  // they keep) copies row u_lo - 1 of the lower band into ring row 0 with
+  // cp.async, P diagonals ahead in the same group as the arc records.  It
+  // checks diagonal s's value during step s, one step before its use,
+  // reading it right after the barrier and testing it at the end of the
+  // step, and polls for it only if it was not written yet when copied.
   const bool gx_top = GX && upper && row == cp.Rc && k == 0;
   const bool gx_halo = GX && lower && threadIdx.x == 0;
   const int uh = bd.u_lo - 1;  // the lower band's top row
   const LV *halo_src = galpha + uh;
-  unsigned long long pend = 0ull;  // bits of (diagonal s - 1, uh), loaded in step s - 1
+  // (q, uh) is a lattice node iff its frame q - uh lies in [0, T_b)
+  auto halo_node = [&](int q) { return q - uh >= 0 && q - uh < bd.Tb && uh <= bd.Ub; };
   int failed = 0;  // a bounded wait of this thread gave up
   auto prefetch = [&](int q) {
     if (MULTI) {
       if (pref) prefetch_diag<REC>(gdiag0, r, q, bd.u_lo, cp.Rc, bd.U1, bd.Tb, bd.Ub, plane);
     } else {
+      // the lower band's value of diagonal q, used at step q + 1
+      if (GX) cp_async8_if(gx_halo && halo_node(q), &r.a(q, 0), halo_src + (long long)q * bd.U1);
       prefetch_rec<REC, G>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
     }
   };
@@ -574,26 +589,6 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
       if (!wait_parity_bounded(r.full((s - 1) & r.mA), ((s - 1) / r.RA) & 1, p.wait_limit))
         failed = 1;
     }
-    if (gx_halo) {
-      if (s >= 1) {
-        // (s - 1, uh) is a node iff its frame s - 1 - uh lies in [0, T_b)
-        LV hv = xf_zero();
-        const int th = s - 1 - uh;
-        if (th >= 0 && th < bd.Tb && uh <= bd.Ub) {
-          unsigned long long w = pend;
-          if (w == 0ull &&
-              !poll_written_bounded(halo_src + (long long)(s - 1) * bd.U1, p.wait_limit, &w))
-            failed = 1;
-          hv = lv_from_bits(w);
-        }
-        r.a(s - 1, 0) = hv;
-      }
-      // the next step's value, in flight while this step computes
-      const int tn = s - uh;
-      pend = (tn >= 0 && tn < bd.Tb && uh <= bd.Ub)
-                 ? ld_relaxed_gpu_bits(halo_src + (long long)s * bd.U1)
-                 : 0ull;
-    }
     // a thread whose wait gave up raises the CTA's abort flag before the
     // barrier (every write to it precedes one), and all leave together after
     // it; a plain barrier and a flag read cost less per diagonal than a
@@ -608,6 +603,9 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     if (MULTI && bd.control && lower && s - 2 - p.max_dur >= 0)
       arrive_cluster_relaxed(map_cta(r.empty((s - 2 - p.max_dur) & r.mA), bd.k - 1));
     if (MULTI && bd.control_warp) continue;
+    // the copy of the lower band's value of diagonal s is complete (every
+    // thread reads it: a broadcast, and no branch)
+    const LV halo_next = GX ? r.a(s, 0) : xf_zero();
     const int t = s - u;
     const bool node = own && u <= bd.Ub && t >= 0 && t < bd.Tb;
     int E[2 * J];
@@ -632,9 +630,29 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     // every lane of the group holds the node's value; lane 0 stores it
     const LV v = node ? (s == 0 ? xf_one() : xf_from_sum(tot, es)) : xf_zero();
     if (own && k == 0) r.a(s, row) = v;
-    if (node && k == 0) {
-      if (!gx_top) galpha[(long long)s * bd.U1 + u] = v;
-      else if (feeds) st_relaxed_gpu_lv(galpha + (long long)s * bd.U1 + u, v);
+    if (GX) {
+      // every node's value with the same gpu-scope relaxed store (the top
+      // row's are polled by the upper band), so no lane branches
+      st_relaxed_gpu_lv_if(node && k == 0 && (feeds || !gx_top),
+                           galpha + (long long)s * bd.U1 + u, v);
+    } else if (node && k == 0) {
+      galpha[(long long)s * bd.U1 + u] = v;
+    }
+    if (GX) {
+      // ring row 0 of diagonal s, read from the next step on: the lower
+      // band's value, polled for (a warp-uniform branch, rarely taken) if it
+      // was not written when copied
+      const bool hn = halo_node(s);
+      if (gx_halo && !hn) r.a(s, 0) = xf_zero();
+      const bool need = gx_halo && hn && !lv_written(halo_next);
+      if (__any_sync(0xffffffffu, need)) {
+        if (need) {
+          LV hv;
+          if (!poll_written_bounded(halo_src + (long long)s * bd.U1, p.wait_limit, &hv))
+            failed = 1;
+          r.a(s, 0) = hv;
+        }
+      }
     }
     if (producer) {
       // publish this diagonal's top row into the upper band's halo slot once
@@ -688,17 +706,21 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
   const bool producer = MULTI && lower && row == 1 && k == 0 && feeds;
   // global exchange, as in the alpha pass: the bottom row's lane 0 stores
   // with gpu-scope relaxed stores, thread 0 (ring row 0 is unused here)
-  // brings row u_lo + Rc of the upper band into ring row Rc + 1
+  // copies row u_lo + Rc of the upper band into ring row Rc + 1
   const bool gx_bottom = GX && lower && row == 1 && k == 0;
   const bool gx_halo = GX && upper && threadIdx.x == 0;
   const int uh = bd.u_lo + cp.Rc;  // the upper band's bottom row
   const LV *halo_src = gbeta + uh;
-  unsigned long long pend = 0ull;  // bits of (diagonal q + 1, uh), loaded in the step before
+  auto halo_node = [&](int q) { return q - uh >= 0 && q - uh < bd.Tb && uh <= bd.Ub; };
   int failed = 0;  // a bounded wait of this thread gave up
   auto prefetch = [&](int q) {
     if (MULTI) {
       if (pref) prefetch_diag<REC>(gdiag0, r, q, bd.u_lo, cp.Rc, bd.U1, bd.Tb, bd.Ub, plane);
     } else {
+      // the upper band's value of diagonal q, used at the step of diagonal q - 1
+      if (GX)
+        cp_async8_if(gx_halo && halo_node(q), &r.a(q, cp.Rc + 1),
+                     halo_src + (long long)q * bd.U1);
       prefetch_rec<REC, G>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
     }
   };
@@ -722,26 +744,6 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
       if (!wait_parity_bounded(r.full((i - 1) & r.mA), ((i - 1) / r.RA) & 1, p.wait_limit))
         failed = 1;
     }
-    if (gx_halo) {
-      if (i >= 1) {
-        // (q + 1, uh) is a node iff its frame q + 1 - uh lies in [0, T_b)
-        LV hv = xf_zero();
-        const int th = q + 1 - uh;
-        if (th >= 0 && th < bd.Tb && uh <= bd.Ub) {
-          unsigned long long w = pend;
-          if (w == 0ull &&
-              !poll_written_bounded(halo_src + (long long)(q + 1) * bd.U1, p.wait_limit, &w))
-            failed = 1;
-          hv = lv_from_bits(w);
-        }
-        r.a(q + 1, cp.Rc + 1) = hv;
-      }
-      // the next step's value (diagonal q), in flight while this step computes
-      const int tn = q - uh;
-      pend = (tn >= 0 && tn < bd.Tb && uh <= bd.Ub)
-                 ? ld_relaxed_gpu_bits(halo_src + (long long)q * bd.U1)
-                 : 0ull;
-    }
     // a thread whose wait gave up raises the CTA's abort flag before the
     // barrier (every write to it precedes one), and all leave together after
     // it; a plain barrier and a flag read cost less per diagonal than a
@@ -756,6 +758,8 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     if (MULTI && bd.control && upper && i - 2 - p.max_dur >= 0)
       arrive_cluster_relaxed(map_cta(r.empty((i - 2 - p.max_dur) & r.mA), bd.k + 1));
     if (MULTI && bd.control_warp) continue;
+    // the copy of the upper band's value of diagonal q is complete
+    const LV halo_next = GX ? r.a(q, cp.Rc + 1) : xf_zero();
     const int t = q - u;
     const bool node = own && u <= bd.Ub && t >= 0 && t < bd.Tb;
     const LV *rec = r.w(q, rowc);
@@ -801,8 +805,26 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
     if (node && k == 0) {
       fr[0] = fb * inv;
       fr[1] = fl * inv;
-      if (!gx_bottom) gbeta[(long long)q * bd.U1 + u] = v;
-      else if (feeds) st_relaxed_gpu_lv(gbeta + (long long)q * bd.U1 + u, v);
+      if (!GX) gbeta[(long long)q * bd.U1 + u] = v;
+    }
+    // every node's value with the same gpu-scope relaxed store (the bottom
+    // row's are polled by the lower band), so no lane branches
+    if (GX)
+      st_relaxed_gpu_lv_if(node && k == 0 && (feeds || !gx_bottom),
+                           gbeta + (long long)q * bd.U1 + u, v);
+    if (GX) {
+      // ring row Rc + 1 of diagonal q, read from the next step on
+      const bool hn = halo_node(q);
+      if (gx_halo && !hn) r.a(q, cp.Rc + 1) = xf_zero();
+      const bool need = gx_halo && hn && !lv_written(halo_next);
+      if (__any_sync(0xffffffffu, need)) {
+        if (need) {
+          LV hv;
+          if (!poll_written_bounded(halo_src + (long long)q * bd.U1, p.wait_limit, &hv))
+            failed = 1;
+          r.a(q, cp.Rc + 1) = hv;
+        }
+      }
     }
     if (producer) {
       // publish this diagonal's bottom row into the lower band's halo slot
