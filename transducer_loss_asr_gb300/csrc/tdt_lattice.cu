@@ -972,9 +972,12 @@ bool cluster_plan(const Problem &p, int K, int X, ClusterPlan *cp) {
   // value ring: max_dur + 2 diagonals in use, the rest is how far a band may
   // run ahead of the band it feeds
   const int RA = pow2_at_least(p.max_dur + 10);
-  // the deeper prefetch for bands without a control warp when its record
-  // ring still fits
-  for (int P : {X != kXCluster ? kPrefetchDeep : kPrefetch, kPrefetch}) {
+  // the deeper prefetch for a single band when its record ring still fits;
+  // global-exchange bands take the shorter one: a band trails the band it
+  // reads by about P diagonals (its neighbour's values are copied P
+  // diagonals ahead), so the last band of a chain of K starts about K P
+  // diagonal steps after the first
+  for (int P : {X == kXNone ? kPrefetchDeep : kPrefetch, kPrefetch}) {
     const int RW = pow2_at_least(P + p.max_dur + 3);
     const size_t bytes = cluster_smem_bytes(RA, RW, Rc, rec);
     if (bytes > kClusterSmemMax) continue;
