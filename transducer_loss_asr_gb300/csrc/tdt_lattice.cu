@@ -640,18 +640,16 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     }
     if (GX) {
       // ring row 0 of diagonal s, read from the next step on: the lower
-      // band's value, polled for (a warp-uniform branch, rarely taken) if it
-      // was not written when copied
+      // band's value, polled for if it was not written when copied (a
+      // branch of thread 0 alone, rarely taken: measured faster than a warp
+      // vote around it)
       const bool hn = halo_node(s);
       if (gx_halo && !hn) r.a(s, 0) = xf_zero();
       const bool need = gx_halo && hn && !lv_written(halo_next);
-      if (__any_sync(0xffffffffu, need)) {
-        if (need) {
-          LV hv;
-          if (!poll_written_bounded(halo_src + (long long)s * bd.U1, p.wait_limit, &hv))
-            failed = 1;
-          r.a(s, 0) = hv;
-        }
+      if (need) {  // thread 0 only, rarely
+        LV hv;
+        if (!poll_written_bounded(halo_src + (long long)s * bd.U1, p.wait_limit, &hv)) failed = 1;
+        r.a(s, 0) = hv;
       }
     }
     if (producer) {
@@ -817,13 +815,10 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
       const bool hn = halo_node(q);
       if (gx_halo && !hn) r.a(q, cp.Rc + 1) = xf_zero();
       const bool need = gx_halo && hn && !lv_written(halo_next);
-      if (__any_sync(0xffffffffu, need)) {
-        if (need) {
-          LV hv;
-          if (!poll_written_bounded(halo_src + (long long)q * bd.U1, p.wait_limit, &hv))
-            failed = 1;
-          r.a(q, cp.Rc + 1) = hv;
-        }
+      if (need) {  // thread 0 only, rarely
+        LV hv;
+        if (!poll_written_bounded(halo_src + (long long)q * bd.U1, p.wait_limit, &hv)) failed = 1;
+        r.a(q, cp.Rc + 1) = hv;
       }
     }
     if (producer) {
