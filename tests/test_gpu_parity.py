@@ -152,7 +152,10 @@ def test_medium_cases(binding, oracle_mod, record_margin, name):
 # Problems whose logits reach 8 MiB go through the chunked multi-stream
 # schedule (up to four chunks of utterances); smaller ones run serially on the
 # caller's stream.  These cases sit above that size: B=5 splits unevenly into
-# chunks of 1,1,1,2 utterances, B=2 into two chunks and B=1 into one.
+# chunks of 1,1,1,2 utterances, B=2 into two chunks and B=1 into one.  The
+# tall ragged case has lattices too tall for one CTA, so each chunk's
+# lattice runs as bands exchanging boundary rows through global memory
+# beside the other chunks' passes, some bands wholly above U_b.
 CHUNKED = {
     "f32_b5_ragged_view": dict(B=5, T=24, U=6, V=8193, blank=8192, durations=(0, 1, 2, 3, 4),
                                dtype="f32", std=1.0, sigma=0.05, reduction="mean_volume",
@@ -164,6 +167,9 @@ CHUNKED = {
                         dtype="f16", std=1.0, sigma=0.02, reduction="sum"),
     "f32_b1_full": dict(B=1, T=50, U=10, V=4097, blank=4096, durations=(0, 1, 2, 3, 4),
                         dtype="f32", std=1.0, sigma=0.0, reduction="none"),
+    "f32_b3_tall_ragged": dict(B=3, T=40, U=700, V=30, blank=29, durations=(0, 1, 2),
+                               dtype="f32", std=1.0, sigma=0.02, reduction="none",
+                               T_range=(20, 40), U_range=(300, 700)),
 }
 
 

@@ -272,9 +272,14 @@ beta_kernel(Problem p, Workspace ws, long long b0) {
 // Diagonals of arc records copied ahead of use: kPrefetchDeep when the
 // record ring fits (single band), else kPrefetch.  At ~0.5-1 us per
 // diagonal either covers the L2/HBM latency; the deeper one also covers it
-// while the streaming passes load HBM.
+// while the streaming passes load HBM.  Global-exchange bands whose launch
+// covers the whole batch take kPrefetchShort: nothing else runs beside
+// such a launch (the node tables are done, the gradient waits for it), and
+// a shorter lead shortens the chain's start-up lag (long_labels lattice
+// 1.614 vs 1.665 ms).
 constexpr int kPrefetch = 4;
 constexpr int kPrefetchDeep = 8;
+constexpr int kPrefetchShort = 2;
 
 // ---- cluster primitives (PTX ISA: mapa, barrier.cluster, st.async); the
 // copy and mbarrier helpers are in tdt_async.cuh
@@ -384,7 +389,7 @@ struct ClusterPlan {
   int Rc;       // lattice rows per CTA
   int G;        // lanes per node
   int RA, RW;   // slots of the value ring and of the record ring (powers of two)
-  int P;        // prefetch distance in diagonals (kPrefetchDeep or kPrefetch)
+  int P;        // prefetch distance in diagonals (kPrefetchDeep, kPrefetch or kPrefetchShort)
   int threads;  // (Rc + 1) * G rounded up to whole warps, plus a control warp for kXCluster
   size_t smem;  // shared bytes used
 };
@@ -953,7 +958,7 @@ constexpr size_t kClusterSmemMax = 220 * 1024;
 
 // Shape of the banded variant for this problem with K bands exchanging by
 // X (K = 1: kXNone), or false.
-bool cluster_plan(const Problem &p, int K, int X, ClusterPlan *cp) {
+bool cluster_plan(const Problem &p, int K, int X, ClusterPlan *cp, bool alone = false) {
   if (p.n_dur > 9) return false;
   if (K == 1) X = kXNone;
   if (K > 1 && X == kXNone) return false;
@@ -968,11 +973,12 @@ bool cluster_plan(const Problem &p, int K, int X, ClusterPlan *cp) {
   // run ahead of the band it feeds
   const int RA = pow2_at_least(p.max_dur + 10);
   // the deeper prefetch for a single band when its record ring still fits;
-  // global-exchange bands take the shorter one: a band trails the band it
-  // reads by about P diagonals (its neighbour's values are copied P
-  // diagonals ahead), so the last band of a chain of K starts about K P
-  // diagonal steps after the first
-  for (int P : {X == kXNone ? kPrefetchDeep : kPrefetch, kPrefetch}) {
+  // global-exchange bands take a shorter one (kPrefetchShort when their
+  // launch runs alone): a band trails the band it reads by about P
+  // diagonals (its neighbour's values are copied P diagonals ahead), so the
+  // last band of a chain of K starts about K P diagonal steps after the first
+  const int P0 = X == kXNone ? kPrefetchDeep : (X == kXGlobal && alone ? kPrefetchShort : kPrefetch);
+  for (int P : {P0, kPrefetch}) {
     const int RW = pow2_at_least(P + p.max_dur + 3);
     const size_t bytes = cluster_smem_bytes(RA, RW, Rc, rec);
     if (bytes > kClusterSmemMax) continue;
@@ -1058,8 +1064,8 @@ cudaError_t launch_cluster_g(const Problem &p, const Workspace &ws, long long b0
       cp.X == kXCluster
           ? lattice_cluster_kernel<ND, G, kXCluster, kPrefetch>
           : cp.X == kXGlobal
-                ? (cp.P == kPrefetchDeep ? lattice_cluster_kernel<ND, G, kXGlobal, kPrefetchDeep>
-                                         : lattice_cluster_kernel<ND, G, kXGlobal, kPrefetch>)
+                ? (cp.P == kPrefetchShort ? lattice_cluster_kernel<ND, G, kXGlobal, kPrefetchShort>
+                                          : lattice_cluster_kernel<ND, G, kXGlobal, kPrefetch>)
                 : (cp.P == kPrefetchDeep ? lattice_cluster_kernel<ND, G, kXNone, kPrefetchDeep>
                                          : lattice_cluster_kernel<ND, G, kXNone, kPrefetch>);
   // at least kLatticeSmemFloor, so no node-table or gradient block shares the SM
@@ -1234,7 +1240,8 @@ cudaError_t launch_lattice(const Problem &p_in, const Workspace &ws, long long b
       // bands exchanging through global memory, as planned for the node
       // tables that cleared their boundary rows
       ClusterPlan cp;
-      if (cluster_plan(p, (int)((p.U1 + p.gx_rows - 1) / p.gx_rows), kXGlobal, &cp) &&
+      const bool alone = nb == p.B;  // the launch covers the whole batch
+      if (cluster_plan(p, (int)((p.U1 + p.gx_rows - 1) / p.gx_rows), kXGlobal, &cp, alone) &&
           cp.Rc == p.gx_rows) {
         bool placed = false;
         const cudaError_t e = launch_cluster_nd(p, ws, g0, nb, with_beta, cp, stream, &placed,
