@@ -336,12 +336,7 @@ enum Exchange {
 // ---- global-memory exchange (PTX ISA memory consistency model: relaxed
 // strong operations at gpu scope; an aligned 64-bit access is single-copy
 // atomic, so a reader sees either the cleared word or the whole value)
-__device__ __forceinline__ void st_relaxed_gpu_lv(LV *p, const LV &v) {
-  const unsigned long long w =
-      (unsigned long long)(unsigned)v.e | ((unsigned long long)__float_as_uint(v.s) << 32);
-  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
-}
-// The same if `pred` (predicated, no branch).
+// 64-bit gpu-scope relaxed store of a value if `pred` (predicated, no branch).
 __device__ __forceinline__ void st_relaxed_gpu_lv_if(bool pred, LV *p, const LV &v) {
   const unsigned long long w =
       (unsigned long long)(unsigned)v.e | ((unsigned long long)__float_as_uint(v.s) << 32);
