@@ -14,6 +14,13 @@ __device__ __forceinline__ unsigned smem_u32(const void *p) {
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem)), "l"(gmem));
 }
+// The same if `pred` (predicated, no branch).
+__device__ __forceinline__ void cp_async16_if(bool pred, void *smem, const void *gmem) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %2, 0;\n\t"
+      "@p cp.async.cg.shared.global [%0], [%1], 16;\n\t}" ::"r"(smem_u32(smem)),
+      "l"(gmem), "r"((int)pred));
+}
 // 8-byte copy global -> shared if `pred` (cp.async.ca: may allocate in L1,
 // which is invalidated at every kernel launch; each address is copied once).
 // Predicated rather than branched around, so that a warp in which one lane

@@ -448,16 +448,31 @@ __device__ __forceinline__ void prefetch_diag(const LV *gdiag0, const ClusterRin
   cp_async_commit();
 }
 
-// One band: each node's lanes copy the node's own record of diagonal q (if
-// it is a lattice node): lane k copies the 16-byte chunks k, k+G, ...; every
-// lane commits one group per call so the group count per step is uniform.
-// (Measured faster than one copying warp when there is no control warp.)
-template <int REC, int G>
+// One band or global-exchange bands: each node's lanes copy the node's own
+// record of diagonal q (if it is a lattice node): lane k copies the 16-byte
+// chunks k, k+G, ...; every lane commits one group per call so the group
+// count per step is uniform.  (Measured faster than one copying warp when
+// there is no control warp.)  PRED: the copies are predicated in a fully
+// unrolled loop, so lanes whose nodes are and are not lattice nodes on
+// diagonal q do not diverge -- faster for global-exchange bands (long_labels
+// lattice 1.61 -> 1.38 ms), slower for one band of five durations
+// (parakeet 0.461 vs 0.416 us per diagonal), which keeps the branch.
+template <int REC, int G, bool PRED>
 __device__ __forceinline__ void prefetch_rec(const LV *gdiag0, const ClusterRings<REC> &r,
                                              int q, int u, int ring_row, int k, int Tb, int Ub,
                                              int U1, bool want) {
   const int t = q - u;
-  if (want && q >= 0 && u >= 0 && u <= Ub && t >= 0 && t < Tb) {
+  const bool copy = want && q >= 0 && u >= 0 && u <= Ub && t >= 0 && t < Tb;
+  if (PRED) {
+    const LV *src = gdiag0 + ((long long)q * U1 + u) * REC;
+    LV *dst = r.w_mut(q, ring_row);
+    constexpr int kChunks = REC / 2;
+#pragma unroll
+    for (int c0 = 0; c0 < kChunks; c0 += G) {
+      const int c = c0 + k;
+      cp_async16_if(copy && c < kChunks, dst + 2 * c, src + 2 * c);
+    }
+  } else if (copy) {
     const LV *src = gdiag0 + ((long long)q * U1 + u) * REC;
     LV *dst = r.w_mut(q, ring_row);
     for (int c = k; c < REC / 2; c += G) cp_async16(dst + 2 * c, src + 2 * c);
@@ -571,7 +586,7 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
     } else {
       // the lower band's value of diagonal q, used at step q + 1
       if (GX) cp_async8_if(gx_halo && halo_node(q), &r.a(q, 0), halo_src + (long long)q * bd.U1);
-      prefetch_rec<REC, G>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
+      prefetch_rec<REC, G, GX>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
     }
   };
   for (int q = 0; q < P; ++q) prefetch(q);
@@ -719,7 +734,7 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
       if (GX)
         cp_async8_if(gx_halo && halo_node(q), &r.a(q, cp.Rc + 1),
                      halo_src + (long long)q * bd.U1);
-      prefetch_rec<REC, G>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
+      prefetch_rec<REC, G, GX>(gdiag0, r, q, u, rowc, k, bd.Tb, bd.Ub, bd.U1, pref);
     }
   };
   // the end state (T_b, U_b), one diagonal past the last: value 1
