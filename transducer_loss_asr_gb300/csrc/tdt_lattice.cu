@@ -1026,11 +1026,15 @@ int preferred_bands(const Problem &p, long long nb) {
   return K < kMaxCluster ? K : kMaxCluster;
 }
 
-// Lanes of a global-exchange band and the CTAs of such a launch.  A band of
-// two warps steps a diagonal about as fast as the one-band lattices of ~40
-// rows, and its neighbour's value reaches it through L2 one step later;
-// the launch takes at most kGlobalBandCtas SMs.
-constexpr int kGlobalBandLanes = 64;
+// Lanes of a global-exchange band (before the cap below) and the CTAs of
+// such a launch: as many small bands as kGlobalBandCtas SMs allow.  A
+// smaller band steps a diagonal faster (long_labels, 1,201 rows, nine
+// durations, per diagonal: 39 bands 0.433 us, 50 0.404, 64 0.394, 76 0.403),
+// and each band takes an SM of its own, so a launch beside other passes
+// keeps to fewer (large_batch's 121-row lattices stay one band: with 2-4
+// global bands the lattice got faster but the step slower, 1.54-1.71 vs
+// 1.44 ms).
+constexpr int kGlobalBandLanes = 32;
 constexpr int kGlobalBandCtas = 128;
 
 }  // namespace
