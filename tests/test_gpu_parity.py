@@ -399,17 +399,33 @@ def test_lattice_bands_do_not_change_results(binding, oracle_mod, record_margin,
 
 # ------------------------------------------------------------- CUDA graphs
 
-@pytest.mark.parametrize("V", [200, 8193], ids=["serial", "chunked"])
+GRAPH_SHAPES = {
+    "serial": dict(V=200, U=6, U_range=(2, 6)),
+    "chunked": dict(V=8193, U=6, U_range=(2, 6)),
+    # lattices too tall for one CTA: bands exchanging boundary rows through
+    # global memory, with their start-order counters and polls, inside the
+    # captured graph (one launch for the batch, and one per chunk)
+    "tall_serial": dict(V=20, U=600, U_range=(300, 600)),
+    "tall_chunked": dict(V=60, U=600, U_range=(300, 600)),
+}
+
+
+@pytest.mark.parametrize("shape", sorted(GRAPH_SHAPES))
 @pytest.mark.parametrize("own_workspace", [True, False])
-def test_cuda_graph_capture_and_replay(binding, own_workspace, V):
+def test_cuda_graph_capture_and_replay(binding, own_workspace, shape):
     """The call is stream-ordered (small problems run on the caller's stream;
     larger ones fork internal streams from it and join them back through
     events), so it can be captured into a CUDA graph; replays give the eager
-    results, also after the inputs change in place.  V=8193 puts the logits
-    above the 8 MiB size of the chunked schedule."""
-    w = scaled(WORKLOADS["tiny"], name="graph", B=3, T=21, U=6, V=V, blank=V - 1,
+    results, also after the inputs change in place.  V=8193 (and the tall
+    case with V=60) put the logits above the 8 MiB size of the chunked
+    schedule."""
+    g = GRAPH_SHAPES[shape]
+    w = scaled(WORKLOADS["tiny"], name="graph", B=3, T=21, U=g["U"], V=g["V"], blank=g["V"] - 1,
                durations=(0, 1, 2, 3, 4), sigma=0.05, reduction="mean_volume",
-               T_range=(10, 21), U_range=(2, 6), seed=606)
+               T_range=(10, 21), U_range=g["U_range"], seed=606)
+    esize = 4
+    chunked = w.B * w.T * (w.U + 1) * w.VD * esize >= 8 << 20
+    assert chunked == shape.endswith("chunked")
     inp = make_inputs(w, device="cuda")
     z = inp["logits"]
     loss = torch.empty(1, dtype=torch.float32, device="cuda")
