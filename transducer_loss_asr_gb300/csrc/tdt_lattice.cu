@@ -566,10 +566,11 @@ __device__ __forceinline__ void alpha_cluster(const Problem &p, const Workspace 
   // so the upper band's bounded wait runs out)
   const bool feeds = !(bd.k == 1 && b == p.fault_utt);
   const bool producer = MULTI && upper && row == cp.Rc && k == 0 && feeds;
-  // global exchange: the top row's lane 0 stores its values with gpu-scope
-  // relaxed stores, and thread 0 (ring row 0, whose lanes compute nothing
-  // they keep) copies row u_lo - 1 of the lower band into ring row 0 with
-  // cp.async, P diagonals ahead in the same group as the arc records.  It
+  // global exchange: every node's value is stored with a gpu-scope relaxed
+  // store (the upper band reads the top row's), and thread 0 (ring row 0,
+  // whose lanes compute nothing they keep) copies row u_lo - 1 of the lower
+  // band into ring row 0 with cp.async, P diagonals ahead in the same group
+  // as the arc records.  It
   // checks diagonal s's value during step s, one step before its use,
   // reading it right after the barrier and testing it at the end of the
   // step, and polls for it only if it was not written yet when copied.
@@ -717,9 +718,10 @@ __device__ __forceinline__ void beta_cluster(const Problem &p, const Workspace &
   // feeds the lower band (testing: band 1 of utterance fault_utt never does)
   const bool feeds = !(bd.k == 1 && b == p.fault_utt);
   const bool producer = MULTI && lower && row == 1 && k == 0 && feeds;
-  // global exchange, as in the alpha pass: the bottom row's lane 0 stores
-  // with gpu-scope relaxed stores, thread 0 (ring row 0 is unused here)
-  // copies row u_lo + Rc of the upper band into ring row Rc + 1
+  // global exchange, as in the alpha pass: gpu-scope relaxed stores of
+  // every node's value (the lower band reads the bottom row's), and thread 0
+  // (ring row 0 is unused here) copies row u_lo + Rc of the upper band into
+  // ring row Rc + 1
   const bool gx_bottom = GX && lower && row == 1 && k == 0;
   const bool gx_halo = GX && upper && threadIdx.x == 0;
   const int uh = bd.u_lo + cp.Rc;  // the upper band's bottom row
