@@ -32,15 +32,17 @@
 //    so neighbouring bands run a few diagonals apart with no cluster-wide
 //    barrier per diagonal.  Every wait is bounded: past the limit the
 //    utterance is marked unusable (NaN loss) and the CTA stops.
-//    Lattices too tall for one CTA instead split into many small bands (two
-//    warps each, ~30 rows) that are not a cluster: a band's boundary row
+//    Lattices too tall for one CTA instead split into many small bands (as
+//    many as a 128-CTA launch allows: long_labels, 1,201 rows, takes 64 of
+//    19 rows per direction) that are not a cluster: a band's boundary row
 //    goes to its neighbour through global memory.  The node-table pass
-//    clears those boundary entries to all-zero bits, which no lattice value
-//    has; the producing lane stores each value with a gpu-scope relaxed
-//    64-bit store, and one thread of the consuming band loads it one step
-//    before it is needed (polling, bounded, when it is not written yet).
-//    CTAs take their band from a start-order ticket, so a band only waits
-//    on bands that started before it.
+//    clears those boundary entries to a marker no lattice value has
+//    (lv_unwritten); node values are stored with gpu-scope relaxed 64-bit
+//    stores, and one thread of the consuming band copies each boundary
+//    value into its ring with the arc records, checks it a step before it
+//    is needed and polls (bounded) only if it was not written yet.  CTAs
+//    take their band from a start-order ticket, so a band only waits on
+//    bands that started before it.
 //  * alpha_kernel / beta_kernel: the same wavefront reading and writing
 //    global memory, any U and D (no limit on label length).
 #include <atomic>
