@@ -399,6 +399,45 @@ def test_lattice_bands_do_not_change_results(binding, oracle_mod, record_margin,
 
 # ------------------------------------------------------------- CUDA graphs
 
+@pytest.mark.parametrize("seed", range(12))
+def test_global_bands_match_one_band_on_random_shapes(binding, seed):
+    """Bands exchanging boundary rows through global memory compute every
+    node with the same arithmetic as one band, so on random shapes (ragged
+    lengths, random duration sets with and without 0, fp32 and bf16) any
+    band count must reproduce bit for bit the result with one band forced
+    (or the fewest cluster bands whose rings fit, for lattices one CTA cannot
+    hold).  Up to 80 bands for up to three utterances is more CTAs than the
+    GPU holds at once: the start-order tickets keep every wait on a CTA that
+    has started."""
+    rng = np.random.default_rng(9000 + seed)
+    T = int(rng.integers(5, 60))
+    U = int(rng.integers(20, 200))
+    V = int(rng.integers(20, 60))
+    nd = int(rng.integers(1, 10))
+    durs = sorted(int(d) for d in rng.choice(np.arange(0, 9), size=nd, replace=False))
+    if max(durs) == 0:
+        durs = [0, 1]
+    B = int(rng.integers(1, 4))
+    dtype = "f32" if seed % 3 else "bf16"
+    w = scaled(WORKLOADS["tiny"], name="gxr%d" % seed, B=B, T=T, U=U, V=V, blank=V - 1,
+               durations=tuple(durs), dtype=dtype, std=1.0, sigma=0.02, reduction="none",
+               T_range=(max(1, T // 2), T), U_range=(U // 2, U), seed=5150 + seed)
+    inp = make_inputs(w, device="cuda")
+    K = int(rng.integers(2, min(80, U + 1) + 1))
+    results = []
+    for bands, mode in ((1, 0), (K, 2)):
+        prev = binding.tdt_loss_set_lattice_bands(bands)
+        prev_mode = binding.tdt_loss_set_lattice_exchange(mode)
+        try:
+            loss, grad = run_gpu(binding, inp)
+        finally:
+            binding.tdt_loss_set_lattice_bands(prev)
+            binding.tdt_loss_set_lattice_exchange(prev_mode)
+        results.append((loss.clone(), grad.clone()))
+    assert torch.equal(results[0][0], results[1][0]), "loss differs with %d global bands" % K
+    assert torch.equal(results[0][1], results[1][1]), "grad differs with %d global bands" % K
+
+
 GRAPH_SHAPES = {
     "serial": dict(V=200, U=6, U_range=(2, 6)),
     "chunked": dict(V=8193, U=6, U_range=(2, 6)),
